@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of the Linformer attention forward on GB300: prints ONE JSON line.
+
+A step is one pass of the whole forward (projection + compressed attention) over
+one batch of the long-sequence workload: b=16, h=12, n=4096, d=64, k=256, one
+layerwise-shared E = F, bf16 in and out, synthetic N(0,1) inputs and N(0,1/k)
+projections.  Throughput is b*h*n tokens per second.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+--impl ours (default): inputs resident in HBM, K steps timed with CUDA events on
+the launching stream, barrier + synchronize on both sides, max over ranks (each
+rank runs its own full batch: weak scaling, no collective on the data path).
+Also reported: the dominant kernel against its roofline (per-kernel CUDA events
+from a second, profiled pass of K steps), the end-to-end rate through the
+host-buffer entry point (copies in the timed region), SM clocks sampled by
+nvidia-smi during the run, and the fp64 oracle timed on the host cores on a
+bounded sample of the same workload.
+
+--impl reference: the fp64 CPU oracle on the host cores, each step a bounded
+sample (whole batches) of the same workload; rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from rank_linear_complexity_gb300.workloads import HEADLINE, WORKLOADS, workload_inputs  # noqa
+
+METRIC = "Linformer attn fwd Mtokens/s at n=4096,k=256 bf16; % of HBM/TC roofline"
+UNIT = "Mtokens/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def algorithmic(w):
+    """Compulsory bytes and algorithmic FLOPs of the forward, and per kernel."""
+    es = 4 if w.dtype == 0 else 2
+    os_ = 2 if w.dtype == 1 else 4
+    units = w.units
+    qkv_each = units * w.n * w.d * es
+    groups = w.h if w.share_mode in (0, 1) else 1
+    n_proj = 2 if w.share_mode in (0, 2) else 1
+    ef = groups * n_proj * w.k * w.n * es
+    o_bytes = units * w.n * w.d * os_
+    flop_proj = 4.0 * w.n * w.k * w.d * units
+    flop_attn = 4.0 * w.n * w.k * w.d * units
+    return {
+        "total_bytes": 3 * qkv_each + ef + o_bytes,
+        "total_flop": flop_proj + flop_attn,
+        "project": {"bytes": 2 * qkv_each + ef, "flop": flop_proj},
+        "attend": {"bytes": qkv_each + o_bytes, "flop": flop_attn},
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the GPU works."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(w, x, units: int, nthreads: int = 0):
+    """Time the oracle on the first `units` units (batch-major); returns
+    (seconds, tokens, threads used)."""
+    from oracle import oracle as orc
+    units = max(1, min(units, w.units))
+    if units < w.h:
+        bsl, hsl = slice(0, 1), slice(0, units)
+    else:
+        bsl, hsl = slice(0, units // w.h), slice(0, w.h)
+        units = (units // w.h) * w.h
+    per_head = w.share_mode in (0, 1)
+    E = x["E"][hsl] if per_head else x["E"]
+    F = None if x["F"] is None else (x["F"][hsl] if per_head else x["F"])
+    args = [x["Q"][bsl, hsl], x["K"][bsl, hsl], x["V"][bsl, hsl], E, F,
+            None if x["lengths"] is None else x["lengths"][bsl]]
+    t0 = time.perf_counter()
+    _, used = orc.linformer_fwd(*args, w.share_mode, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, units * w.n, used
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = HEADLINE
+    from oracle import oracle as orc
+    orc.build()
+    x = workload_inputs(w)
+    # Size each step so that warm-up + timed steps take about REF_BUDGET_S seconds.
+    t_unit, _, _ = oracle_sample(w, x, 1)
+    per_step = args.ref_budget_s / (args.steps + args.warmup)
+    units = int(max(1, min(w.units, per_step / max(t_unit, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample(w, x, units)
+    times, used, tokens = [], 1, 0
+    for _ in range(args.steps):
+        dt, tokens, used = oracle_sample(w, x, units)
+        times.append(dt)
+    total = sum(times)
+    value = tokens * len(times) / total / 1e6
+    sample = (f"{tokens // w.n} of {w.units} units ({tokens} tokens) per step, fp64 oracle, "
+              f"OpenMP on {used} threads of {host_cores()} host cores")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": w.describe(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import rank_linear_complexity_gb300.linformer as lf
+    from rank_linear_complexity_gb300 import build as libbuild
+    libbuild.build()
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload] if args.workload is not None else HEADLINE
+    x = workload_inputs(w)
+    g = {kk: (v.to(dev) if v is not None else None) for kk, v in x.items()}
+    out_dt = torch.bfloat16 if w.dtype == 1 else torch.float32
+    O = torch.empty((w.b, w.h, w.n, w.d), dtype=out_dt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        st = lf.linformer_attn_fwd(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], O,
+                                   w.b, w.h, w.n, w.d, w.k, w.share_mode, w.dtype, stream)
+        if st != 0:
+            raise lf.LinformerError(st, "linformer_attn_fwd")
+
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if lf.linformer_debug_read_device_status(stream) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # --- headline: K steps, CUDA events on the launching stream -----------------------
+    launches0 = lf.linformer_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = lf.linformer_launch_count() - launches0
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
+    clocks = sampler.stop()
+    ms_step = ms_total / args.steps
+    value = world * w.tokens / (ms_step * 1e-3) / 1e6
+
+    # --- per-kernel durations: a second pass of K steps with library events -----------
+    lf.linformer_profile_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    lf.linformer_profile_enable(False)
+    per_kernel = lf.linformer_profile_collect()
+    if lf.linformer_debug_read_device_status(stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    peaks = load_peaks()
+    alg = algorithmic(w)
+    kernels = {}
+    for name, (ms, cnt) in per_kernel.items():
+        part = "project" if "project" in name else "attend"
+        avg_s = ms / cnt * 1e-3
+        t_mem = alg[part]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        t_tc = alg[part]["flop"] / (peaks["bf16_tflops"] * 1e12)
+        bound = "hbm" if t_mem >= t_tc else "tensor"
+        if bound == "hbm":
+            achieved, peak, unit = alg[part]["bytes"] / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
+        else:
+            achieved, peak, unit = alg[part]["flop"] / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        kernels[name] = {"avg_us": avg_s * 1e6, "launches": cnt, "bound": bound,
+                         "achieved": achieved, "peak": peak, "unit": unit,
+                         "frac": achieved / peak}
+    dominant = max(kernels, key=lambda k: kernels[k]["avg_us"]) if kernels else None
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if dominant and os.path.exists(tfile):
+        try:
+            traffic = json.load(open(tfile)).get(dominant)
+        except Exception:
+            traffic = None
+    roofline = None
+    if dominant:
+        kd = kernels[dominant]
+        roofline = {"kernel": dominant, "bound": kd["bound"], "achieved": kd["achieved"],
+                    "peak": kd["peak"], "unit": kd["unit"], "frac": kd["frac"],
+                    "traffic": traffic, "peak_source": peaks["source"] + " (burst)"}
+    t_roof = max(alg["total_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                 alg["total_flop"] / (peaks["bf16_tflops"] * 1e12))
+    path_frac = t_roof / (ms_step * 1e-3)
+
+    # --- end to end through the host-buffer entry point -------------------------------
+    e2e = None
+    if not args.no_e2e:
+        pin = {kk: (v.pin_memory() if v is not None else None) for kk, v in x.items()}
+        Oh = torch.empty((w.b, w.h, w.n, w.d), dtype=out_dt).pin_memory()
+
+        def host_step():
+            st = lf.linformer_attn_fwd_host(pin["Q"], pin["K"], pin["V"], pin["E"], pin["F"],
+                                            pin["lengths"], Oh, w.b, w.h, w.n, w.d, w.k,
+                                            w.share_mode, w.dtype, stream)
+            if st != 0:
+                raise lf.LinformerError(st, "linformer_attn_fwd_host")
+
+        for _ in range(min(3, args.warmup)):
+            host_step()
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            host_step()
+        dt = max_over_ranks(time.perf_counter() - t0, world)
+        h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+        e2e = {"value": world * w.tokens * e2e_steps / dt / 1e6, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": Oh.numel() * Oh.element_size(),
+               "steps": e2e_steps, "ms_per_step": 1e3 * dt / e2e_steps}
+
+    # --- CPU baseline: the oracle on a bounded sample, rank 0 at N = 1 -----------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, tokens, used = oracle_sample(w, x, args.cpu_units)
+        cpu = {"value": tokens / dt / 1e6, "unit": UNIT, "cores": used, "kind": "oracle",
+               "sample": f"first {tokens // w.n} of {w.units} units ({tokens} tokens), one pass, "
+                         f"{dt:.2f} s wall, {used} OpenMP threads on {host_cores()} host cores"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype != 0 else "f32", "data": "synthetic",
+            "config": dict(w.describe(), parallelism=f"replicas{world}",
+                           l2=("no flush: inputs larger than L2 "
+                               f"(Q+K+V {3 * w.tokens * w.d * 2 / 1e6:.0f} MB vs "
+                               f"{L2_BYTES / 1e6:.0f} MB L2)")),
+            "tflops": alg["total_flop"] / (ms_step * 1e-3) / 1e12,
+            "path_roofline_frac": path_frac,
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=None,
+                    help="index into the workload table (default: the n=4096, k=256 case)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-units", type=int, default=48,
+                    help="units of the workload the CPU-baseline oracle pass covers")
+    ap.add_argument("--ref-budget-s", type=float, default=90.0,
+                    help="--impl reference: seconds for all warm-up + timed steps")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

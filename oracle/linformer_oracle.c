@@ -44,17 +44,21 @@ enum { OR_PER_HEAD = 0, OR_KV = 1, OR_HEADWISE = 2, OR_LAYERWISE = 3 };
 
 /* Kbar[j][c] = sum_{t < L} Ehat[j][t] * X[t][c]   (Ehat: k x n row-major, X: n x d)
  * Rows t >= L of X are never read: they count as zero whatever they hold. */
+static void project_row(int n, int d, int j, int L, const double *Ehat, const double *X,
+                        double *Xbar)
+{
+    for (int c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int t = 0; t < L; ++t)
+            acc += Ehat[(int64_t)j * n + t] * X[(int64_t)t * d + c];
+        Xbar[(int64_t)j * d + c] = acc;
+    }
+}
+
 void oracle_project(int n, int d, int k, int L, const double *Ehat, const double *X,
                     double *Xbar)
 {
-    for (int j = 0; j < k; ++j) {
-        for (int c = 0; c < d; ++c) {
-            double acc = 0.0;
-            for (int t = 0; t < L; ++t)
-                acc += Ehat[(int64_t)j * n + t] * X[(int64_t)t * d + c];
-            Xbar[(int64_t)j * d + c] = acc;
-        }
-    }
+    for (int j = 0; j < k; ++j) project_row(n, d, j, L, Ehat, X, Xbar);
 }
 
 /* One query row i (0 <= i < n) of the compressed attention.
@@ -140,21 +144,23 @@ int oracle_linformer_fwd(const double *Q, const double *K, const double *V,
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #endif
-    /* Step 1: projections, one unit per iteration. */
+    /* Step 1: projections, one projected row of one unit per iteration. */
 #pragma omp parallel
     {
 #ifdef _OPENMP
 #pragma omp single
         used = omp_get_num_threads();
 #endif
-#pragma omp for schedule(dynamic, 1)
-        for (int64_t u = 0; u < units; ++u) {
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t uj = 0; uj < units * k; ++uj) {
+            const int64_t u = uj / k;
+            const int j = (int)(uj % k);
             const int batch = (int)(u / h), head = (int)(u % h);
             const int L = valid_length(pad_lengths, batch, n);
             const double *Eh, *Fh;
             pick_projections(share_mode, head, k, n, E, F, &Eh, &Fh);
-            oracle_project(n, d, k, L, Eh, K + u * nd, Kb + u * kd);
-            oracle_project(n, d, k, L, Fh, V + u * nd, Vb + u * kd);
+            project_row(n, d, j, L, Eh, K + u * nd, Kb + u * kd);
+            project_row(n, d, j, L, Fh, V + u * nd, Vb + u * kd);
         }
         /* Step 2: compressed attention, one query row per iteration. */
         double *s = (double *)malloc(sizeof(double) * (size_t)k);

@@ -1,0 +1,60 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "linformer_attn.h"
+
+namespace linformer {
+
+// One call's arguments, already validated.
+struct Problem {
+    const void *Q, *K, *V, *E, *F;
+    const int32_t *pad;
+    void *O;
+    int b, h, n, d, k, share_mode, dtype;
+    cudaStream_t stream;
+
+    int64_t units() const { return (int64_t)b * h; }
+    // E (and F) carry a leading head index in these modes.
+    bool proj_per_head() const {
+        return share_mode == LINFORMER_SHARE_PER_HEAD || share_mode == LINFORMER_SHARE_KV;
+    }
+    // F is its own tensor (not E) in these modes.
+    bool distinct_f() const {
+        return share_mode == LINFORMER_SHARE_PER_HEAD || share_mode == LINFORMER_SHARE_HEADWISE;
+    }
+    const void *f_or_e() const { return distinct_f() ? F : E; }
+    size_t in_elem() const { return dtype == LINFORMER_F32 ? 4 : 2; }
+    size_t out_elem() const { return dtype == LINFORMER_BF16 ? 2 : 4; }
+};
+
+// Brackets one kernel launch: counts it and, while profiling is on, records CUDA
+// events around it on its stream.
+class KernelScope {
+  public:
+    KernelScope(int kernel_id, cudaStream_t s);
+    ~KernelScope();
+
+  private:
+    int id_;
+    cudaStream_t s_;
+    cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
+// Device status word of the current device (set by bounded waits that ran out).
+int *device_status_ptr();
+
+// Process-wide P.Vbar product-count setting (0 = automatic, 1 or 3).
+int pv_terms_setting();
+
+// fp32 SIMT kernels (simt_kernels.cu).
+int simt_project(const Problem &p, float *Kbar, float *Vbar);
+int simt_attend(const Problem &p, const float *Kbar, const float *Vbar);
+
+// Tensor-core kernels (tc_project.cu, tc_attend.cu).
+bool tc_supported(int n, int d, int k, int dtype);
+int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out);
+
+}  // namespace linformer

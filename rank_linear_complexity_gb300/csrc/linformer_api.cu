@@ -1,0 +1,281 @@
+// Host side of the C ABI declared in include/linformer_attn.h: argument
+// validation, path selection, stream-ordered workspace, launch bookkeeping,
+// profiling events and the device status word.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.cuh"
+
+namespace linformer {
+
+// Set to a non-zero code by a kernel whose bounded wait ran out.
+__device__ int g_device_status;
+
+namespace {
+
+std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_profiling{0};
+std::atomic<int> g_pv_terms{0};
+
+struct ProfileRecord {
+    int id;
+    cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+std::vector<ProfileRecord> g_prof;
+
+constexpr int kMaxDevices = 64;
+int *g_status_addr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape, enum and F rules shared by every entry point.
+int validate_common(int b, int h, int n, int d, int k, int share_mode, int dtype) {
+    if (b < 1 || h < 1 || n < 1 || d < 1 || k < 1) return LINFORMER_ERR_SIZE;
+    if (share_mode < LINFORMER_SHARE_PER_HEAD || share_mode > LINFORMER_SHARE_LAYERWISE)
+        return LINFORMER_ERR_ENUM;
+    if (dtype < LINFORMER_F32 || dtype > LINFORMER_BF16_F32OUT) return LINFORMER_ERR_ENUM;
+    if (d > 128 || k > 1024) return LINFORMER_ERR_UNSUPPORTED;
+    const int64_t units = (int64_t)b * h;
+    if (units > (1LL << 31) - 1) return LINFORMER_ERR_SIZE;
+    if (units * (int64_t)n > (1LL << 40) || units * (int64_t)n * d > (1LL << 46))
+        return LINFORMER_ERR_SIZE;
+    return LINFORMER_OK;
+}
+
+int validate_f(int share_mode, const void *E, const void *F) {
+    const bool distinct = share_mode == LINFORMER_SHARE_PER_HEAD ||
+                          share_mode == LINFORMER_SHARE_HEADWISE;
+    if (distinct && !F) return LINFORMER_ERR_F_MODE;
+    if (!distinct && F && F != E) return LINFORMER_ERR_F_MODE;
+    return LINFORMER_OK;
+}
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int select_path(int n, int d, int k, int dtype) {
+    return tc_supported(n, d, k, dtype) ? LINFORMER_PATH_TENSOR : LINFORMER_PATH_SIMT;
+}
+
+// The forward on device pointers (arguments already validated).  Kbar_out and
+// Vbar_out, when non-null, receive the fp32 projections and O is not computed.
+int run_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
+    if (select_path(p.n, p.d, p.k, p.dtype) == LINFORMER_PATH_TENSOR)
+        return tc_forward(p, Kbar_out, Vbar_out);
+    float *Kb = Kbar_out, *Vb = Vbar_out;
+    void *ws = nullptr;
+    const size_t bytes = (size_t)p.units() * p.k * p.d * sizeof(float);
+    if (!Kb) {
+        if (cudaMallocAsync(&ws, 2 * bytes, p.stream) != cudaSuccess) {
+            cudaGetLastError();
+            return LINFORMER_ERR_ALLOC;
+        }
+        Kb = static_cast<float *>(ws);
+        Vb = reinterpret_cast<float *>(static_cast<char *>(ws) + bytes);
+    }
+    int st = simt_project(p, Kb, Vb);
+    if (st == LINFORMER_OK && !Kbar_out) st = simt_attend(p, Kb, Vb);
+    if (ws) cudaFreeAsync(ws, p.stream);
+    return st;
+}
+
+}  // namespace
+
+KernelScope::KernelScope(int kernel_id, cudaStream_t s) : id_(kernel_id), s_(s) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (g_profiling.load(std::memory_order_relaxed)) {
+        if (cudaEventCreate(&a_) == cudaSuccess && cudaEventCreate(&b_) == cudaSuccess) {
+            cudaEventRecord(a_, s_);
+        } else {
+            a_ = b_ = nullptr;
+        }
+    }
+}
+
+KernelScope::~KernelScope() {
+    if (!a_) return;
+    cudaEventRecord(b_, s_);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof.push_back({id_, a_, b_});
+}
+
+int *device_status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<int *>(ptr);
+    }
+    return g_status_addr[dev];
+}
+
+int pv_terms_setting() { return g_pv_terms.load(std::memory_order_relaxed); }
+
+}  // namespace linformer
+
+using namespace linformer;
+
+extern "C" int linformer_attn_fwd(const void *Q, const void *K, const void *V, const void *E,
+                                  const void *F, const int32_t *pad_lengths, void *O, int b,
+                                  int h, int n, int d, int k, int share_mode, int dtype,
+                                  void *stream) {
+    if (!Q || !K || !V || !E || !O) return LINFORMER_ERR_NULL;
+    int st = validate_common(b, h, n, d, k, share_mode, dtype);
+    if (st) return st;
+    if ((st = validate_f(share_mode, E, F))) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(E) || !aligned16(O) ||
+        (F && !aligned16(F)) || (reinterpret_cast<uintptr_t>(pad_lengths) & 3u))
+        return LINFORMER_ERR_ALIGN;
+    Problem p{Q, K, V, E, F, pad_lengths, O, b, h, n, d, k, share_mode, dtype,
+              as_stream(stream)};
+    return run_forward(p, nullptr, nullptr);
+}
+
+extern "C" int linformer_project_fwd(const void *K, const void *V, const void *E,
+                                     const void *F, const int32_t *pad_lengths, float *Kbar,
+                                     float *Vbar, int b, int h, int n, int d, int k,
+                                     int share_mode, int dtype, void *stream) {
+    if (!K || !V || !E || !Kbar || !Vbar) return LINFORMER_ERR_NULL;
+    int st = validate_common(b, h, n, d, k, share_mode, dtype);
+    if (st) return st;
+    if ((st = validate_f(share_mode, E, F))) return st;
+    if (!aligned16(K) || !aligned16(V) || !aligned16(E) || !aligned16(Kbar) ||
+        !aligned16(Vbar) || (F && !aligned16(F)) ||
+        (reinterpret_cast<uintptr_t>(pad_lengths) & 3u))
+        return LINFORMER_ERR_ALIGN;
+    Problem p{nullptr, K, V, E, F, pad_lengths, nullptr, b, h, n, d, k, share_mode, dtype,
+              as_stream(stream)};
+    return run_forward(p, Kbar, Vbar);
+}
+
+extern "C" int linformer_attn_fwd_host(const void *Q, const void *K, const void *V,
+                                       const void *E, const void *F,
+                                       const int32_t *pad_lengths, void *O, int b, int h,
+                                       int n, int d, int k, int share_mode, int dtype,
+                                       void *stream) {
+    if (!Q || !K || !V || !E || !O) return LINFORMER_ERR_NULL;
+    int st = validate_common(b, h, n, d, k, share_mode, dtype);
+    if (st) return st;
+    if ((st = validate_f(share_mode, E, F))) return st;
+    const bool distinct = share_mode == LINFORMER_SHARE_PER_HEAD ||
+                          share_mode == LINFORMER_SHARE_HEADWISE;
+    const bool per_head = share_mode == LINFORMER_SHARE_PER_HEAD ||
+                          share_mode == LINFORMER_SHARE_KV;
+    const size_t in_e = dtype == LINFORMER_F32 ? 4 : 2;
+    const size_t out_e = dtype == LINFORMER_BF16 ? 2 : 4;
+    const size_t qkv = (size_t)b * h * n * d * in_e;
+    const size_t proj = (size_t)(per_head ? h : 1) * k * n * in_e;
+    const size_t obytes = (size_t)b * h * n * d * out_e;
+    const size_t pbytes = pad_lengths ? (size_t)b * sizeof(int32_t) : 0;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t total = 3 * up(qkv) + up(proj) * (distinct ? 2 : 1) + up(obytes) + up(pbytes);
+    cudaStream_t s = as_stream(stream);
+    char *base = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&base), total, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LINFORMER_ERR_ALLOC;
+    }
+    char *dQ = base, *dK = dQ + up(qkv), *dV = dK + up(qkv), *dE = dV + up(qkv);
+    char *dF = distinct ? dE + up(proj) : nullptr;
+    char *dO = (distinct ? dF : dE) + up(proj);
+    char *dP = pad_lengths ? dO + up(obytes) : nullptr;
+    bool ok = cudaMemcpyAsync(dQ, Q, qkv, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+              cudaMemcpyAsync(dK, K, qkv, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+              cudaMemcpyAsync(dV, V, qkv, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+              cudaMemcpyAsync(dE, E, proj, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+              (!dF || cudaMemcpyAsync(dF, F, proj, cudaMemcpyHostToDevice, s) == cudaSuccess) &&
+              (!dP || cudaMemcpyAsync(dP, pad_lengths, pbytes, cudaMemcpyHostToDevice, s) ==
+                          cudaSuccess);
+    st = ok ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
+    if (st == LINFORMER_OK) {
+        Problem p{dQ, dK, dV, dE, dF, reinterpret_cast<const int32_t *>(dP), dO, b, h, n, d,
+                  k, share_mode, dtype, s};
+        st = run_forward(p, nullptr, nullptr);
+    }
+    if (st == LINFORMER_OK &&
+        cudaMemcpyAsync(O, dO, obytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        st = LINFORMER_ERR_LAUNCH;
+    cudaFreeAsync(base, s);
+    if (cudaStreamSynchronize(s) != cudaSuccess && st == LINFORMER_OK) st = LINFORMER_ERR_LAUNCH;
+    return st;
+}
+
+extern "C" int linformer_select_path(int b, int h, int n, int d, int k, int share_mode,
+                                     int dtype) {
+    int st = validate_common(b, h, n, d, k, share_mode, dtype);
+    if (st) return st;
+    return select_path(n, d, k, dtype);
+}
+
+extern "C" const char *linformer_status_string(int status) {
+    switch (status) {
+        case LINFORMER_OK: return "ok";
+        case LINFORMER_ERR_NULL: return "a required pointer is NULL";
+        case LINFORMER_ERR_SIZE: return "bad size (b, h, n, d, k must be >= 1 and fit)";
+        case LINFORMER_ERR_UNSUPPORTED: return "unsupported shape (d <= 128, k <= 1024)";
+        case LINFORMER_ERR_ENUM: return "bad share_mode or dtype";
+        case LINFORMER_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case LINFORMER_ERR_F_MODE: return "F inconsistent with the sharing mode";
+        case LINFORMER_ERR_ALLOC: return "workspace allocation failed";
+        case LINFORMER_ERR_LAUNCH: return "CUDA call or kernel launch failed";
+        case LINFORMER_ERR_DEVICE: return "device-side bounded wait ran out";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int linformer_debug_read_device_status(void *stream) {
+    cudaStream_t s = as_stream(stream);
+    int *addr = device_status_ptr();
+    if (!addr) return LINFORMER_ERR_LAUNCH;
+    int value = 0;
+    if (cudaMemcpyAsync(&value, addr, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(addr, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return LINFORMER_ERR_LAUNCH;
+    return value ? LINFORMER_ERR_DEVICE : LINFORMER_OK;
+}
+
+extern "C" int linformer_set_pv_terms(int terms) {
+    if (terms != 0 && terms != 1 && terms != 3) return LINFORMER_ERR_ENUM;
+    return g_pv_terms.exchange(terms);
+}
+
+extern "C" int64_t linformer_launch_count(void) { return g_launches.load(); }
+
+extern "C" int linformer_profile_enable(int enable) {
+    return g_profiling.exchange(enable ? 1 : 0);
+}
+
+extern "C" int linformer_profile_collect(double *ms, int64_t *launches) {
+    std::vector<ProfileRecord> recs;
+    {
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        recs.swap(g_prof);
+    }
+    int st = LINFORMER_OK;
+    for (auto &r : recs) {
+        float t = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess ||
+            cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+            st = LINFORMER_ERR_LAUNCH;
+        if (r.id >= 0 && r.id < LINFORMER_KERNEL_COUNT) {
+            if (ms) ms[r.id] += t;
+            if (launches) launches[r.id] += 1;
+        }
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    return st;
+}
+
+extern "C" const char *linformer_kernel_name(int id) {
+    static const char *names[LINFORMER_KERNEL_COUNT] = {
+        "tc_project_kernel", "tc_attend_kernel", "simt_project_kernel", "simt_attend_kernel"};
+    return (id >= 0 && id < LINFORMER_KERNEL_COUNT) ? names[id] : nullptr;
+}

@@ -214,11 +214,11 @@ MUTANTS = {
     "scale_1_over_d": ("const double scale = 1.0 / sqrt((double)d);\n    const double *q",
                        "const double scale = 1.0 / (double)d;\n    const double *q"),
     "transposed_E": ("acc += Ehat[(int64_t)j * n + t] * X[(int64_t)t * d + c];",
-                     "acc += Ehat[(int64_t)t * k + j] * X[(int64_t)t * d + c];"),
+                     "acc += Ehat[(int64_t)t * n + j] * X[(int64_t)t * d + c];"),
     "F_replaced_by_E": ("*Fh = (share_mode == OR_KV || share_mode == OR_LAYERWISE) ? *Eh : F + off;",
                         "*Fh = *Eh;"),
-    "padding_ignored_in_projection": ("for (int t = 0; t < L; ++t)\n                acc +=",
-                                      "for (int t = 0; t < n; ++t)\n                acc +="),
+    "padding_ignored_in_projection": ("for (int t = 0; t < L; ++t)\n            acc +=",
+                                      "for (int t = 0; t < n; ++t)\n            acc +="),
     "padded_queries_not_zeroed": ("    if (i >= L) {\n        for (int c = 0; c < d; ++c) Orow[c] = 0.0;",
                                   "    if (0) {\n        for (int c = 0; c < d; ++c) Orow[c] = 0.0;"),
     "missing_normalisation": ("for (int j = 0; j < k; ++j) s[j] /= sum;", ""),

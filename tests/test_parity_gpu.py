@@ -1,0 +1,186 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Small cases are compared element by element over the whole output; the five
+evaluation workloads run at full size in the same call the benchmark times and
+are compared on sampled units and rows (the oracle computes those one by one),
+plus properties that hold at any size (finite values, zero padded rows).
+"""
+import numpy as np
+import pytest
+import torch
+
+import rank_linear_complexity_gb300.linformer as lf
+from oracle import oracle as orc
+from rank_linear_complexity_gb300.workloads import (BF16, BF16_F32OUT, F32, HEADWISE, KV,
+                                                    LAYERWISE, PER_HEAD, WORKLOADS,
+                                                    workload_inputs)
+from tests.parity import case_inputs, check, host64, to_device
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def run(x, share_mode, dtype):
+    g = to_device(x, DEV)
+    O = lf.attention(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], share_mode,
+                     out_fp32=(dtype == BF16_F32OUT))
+    torch.cuda.synchronize()
+    assert lf.linformer_debug_read_device_status() == 0
+    return O
+
+
+def oracle_full(x, share_mode):
+    O, _ = orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"], share_mode)
+    return O
+
+
+def with_dtype(x, dtype):
+    return x
+
+
+# --- small and edge shapes, whole output compared ------------------------------------
+
+SMALL = [
+    # (b, h, n, d, k, share_mode, dtype, ragged)
+    (2, 4, 512, 64, 128, PER_HEAD, F32, False),       # the fp32 evaluation workload
+    (2, 3, 320, 64, 128, LAYERWISE, BF16, False),     # 2.5 query tiles
+    (2, 3, 320, 64, 256, PER_HEAD, BF16, True),
+    (1, 4, 1000, 64, 64, KV, BF16, False),
+    (3, 2, 777, 64, 96, HEADWISE, BF16_F32OUT, True),
+    (2, 2, 384, 64, 200, HEADWISE, BF16, False),
+    (1, 2, 300, 32, 40, PER_HEAD, BF16, False),       # d != 64: SIMT kernels
+    (1, 2, 130, 128, 300, KV, F32, False),            # k > 256 on SIMT
+    (2, 2, 250, 64, 64, LAYERWISE, BF16, True),       # n not a multiple of 8
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"b{c[0]}h{c[1]}n{c[2]}d{c[3]}k{c[4]}m{c[5]}t{c[6]}"
+                                             f"{'r' if c[7] else ''}" for c in SMALL])
+def test_small_cases_match_oracle(case):
+    b, h, n, d, k, mode, dtype, ragged = case
+    x = case_inputs(b, h, n, d, k, mode, dtype, ragged=ragged, seed=hash(case) % 1000)
+    O = run(x, mode, dtype)
+    check(host64(O), oracle_full(x, mode), dtype, str(case))
+
+
+EDGE_N = [1, 2, 3, 5, 8, 127, 129, 136]
+EDGE_K = [1, 2, 16, 64, 255, 256]
+
+
+@pytest.mark.parametrize("n", EDGE_N)
+@pytest.mark.parametrize("k", EDGE_K)
+def test_edge_shapes(n, k):
+    idx = EDGE_N.index(n) * len(EDGE_K) + EDGE_K.index(k)
+    mode = idx % 4
+    dtype = (BF16, BF16_F32OUT, BF16, F32)[idx % 4]
+    x = case_inputs(2, 2, n, 64, k, mode, dtype, seed=idx)
+    O = run(x, mode, dtype)
+    check(host64(O), oracle_full(x, mode), dtype, f"n={n} k={k} mode={mode}")
+
+
+@pytest.mark.parametrize("n", [8, 136, 256])
+def test_k_equals_n(n):
+    x = case_inputs(1, 2, n, 64, n if n <= 256 else 256, PER_HEAD, BF16, seed=n)
+    O = run(x, PER_HEAD, BF16)
+    check(host64(O), oracle_full(x, PER_HEAD), BF16, f"k=n={n}")
+
+
+@pytest.mark.parametrize("mode", [PER_HEAD, KV, HEADWISE, LAYERWISE])
+@pytest.mark.parametrize("dtype", [BF16, F32])
+def test_lengths_edges(mode, dtype):
+    n = 200
+    x = case_inputs(4, 2, n, 64, 64, mode, dtype, seed=5 + mode, lengths=[0, 1, n - 1, n])
+    O = run(x, mode, dtype)
+    ref = oracle_full(x, mode)
+    check(host64(O), ref, dtype, f"lengths mode={mode}")
+    assert (host64(O)[0] == 0).all() and (host64(O)[1, :, 1:] == 0).all()
+
+
+# --- invariants on the GPU -----------------------------------------------------------
+
+def test_padded_rows_cannot_leak():
+    n = 640
+    x = case_inputs(3, 2, n, 64, 128, PER_HEAD, BF16, seed=9, lengths=[640, 333, 129])
+    O1 = run(x, PER_HEAD, BF16)
+    y = {kk: (v.clone() if v is not None else None) for kk, v in x.items()}
+    for bi, L in enumerate([640, 333, 129]):
+        y["K"][bi, :, L:] = float("nan")
+        y["V"][bi, :, L:] = float("inf")
+        y["Q"][bi, :, L:] = float("nan")
+    O2 = run(y, PER_HEAD, BF16)
+    assert torch.equal(O1, O2)
+
+
+def test_deterministic_bitwise():
+    x = case_inputs(4, 3, 1024, 64, 256, LAYERWISE, BF16, seed=11)
+    O1 = run(x, LAYERWISE, BF16)
+    O2 = run(x, LAYERWISE, BF16)
+    assert torch.equal(O1, O2)
+
+
+def test_sharing_mode_consistency():
+    x = case_inputs(2, 3, 512, 64, 128, HEADWISE, BF16, seed=12)
+    O_hw = run(x, HEADWISE, BF16)
+    y = dict(x)
+    y["E"] = x["E"].unsqueeze(0).repeat(3, 1, 1).contiguous()
+    y["F"] = x["F"].unsqueeze(0).repeat(3, 1, 1).contiguous()
+    O_ph = run(y, PER_HEAD, BF16)
+    check(host64(O_ph), host64(O_hw), BF16, "per-head with equal E_h vs headwise")
+    z = dict(x)
+    z["F"] = None
+    O_lw = run(z, LAYERWISE, BF16)
+    w = dict(x)
+    w["F"] = x["E"]
+    O_hw2 = run(w, HEADWISE, BF16)
+    check(host64(O_lw), host64(O_hw2), BF16, "layerwise vs headwise with F = E")
+
+
+@pytest.mark.parametrize("mode", [PER_HEAD, KV, HEADWISE, LAYERWISE])
+def test_projection_entry_point(mode):
+    x = case_inputs(2, 3, 1000, 64, 128, mode, BF16, ragged=True, seed=20 + mode)
+    g = to_device(x, DEV)
+    Kb, Vb = lf.projection(g["K"], g["V"], g["E"], g["F"], g["lengths"], mode)
+    torch.cuda.synchronize()
+    _, _, rK, rV = orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"], mode,
+                                     return_proj=True)
+    for got, ref in ((host64(Kb), rK), (host64(Vb), rV)):
+        assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max() + 1e-6
+
+
+def test_host_entry_point_matches_device():
+    x = case_inputs(2, 2, 512, 64, 128, KV, BF16, seed=30)
+    O_dev = run(x, KV, BF16)
+    pin = {kk: (v.pin_memory() if v is not None else None) for kk, v in x.items()}
+    O_host = torch.empty(O_dev.shape, dtype=torch.bfloat16).pin_memory()
+    st = lf.linformer_attn_fwd_host(pin["Q"], pin["K"], pin["V"], pin["E"], None, None, O_host,
+                                    2, 2, 512, 64, 128, KV, BF16)
+    assert st == 0, lf.status_string(st)
+    assert torch.equal(O_host, O_dev.cpu())
+
+
+# --- the five evaluation workloads at full size, sampled ------------------------------
+
+def sample_rows(n, L, rng, count=192):
+    picks = {0, n - 1, max(0, L - 1), min(n - 1, L), 127, 128, min(n - 1, 129)}
+    picks.update(rng.integers(0, n, size=count).tolist())
+    return np.array(sorted(p for p in picks if 0 <= p < n), np.int64)
+
+
+@pytest.mark.parametrize("wi", range(len(WORKLOADS)), ids=[w.name for w in WORKLOADS])
+def test_workload_full_size_sampled(wi):
+    w = WORKLOADS[wi]
+    x = workload_inputs(w)
+    O = run(x, w.share_mode, w.dtype)
+    assert torch.isfinite(O.float()).all()
+    rng = np.random.default_rng(wi)
+    lengths = x["lengths"].numpy() if x["lengths"] is not None else np.full(w.b, w.n)
+    for bi in range(w.b):
+        assert (O[bi, :, int(lengths[bi]):] == 0).all()
+    units = {(0, 0), (w.b - 1, w.h - 1)}
+    units.update((int(rng.integers(w.b)), int(rng.integers(w.h))) for _ in range(2))
+    for (bi, hi) in sorted(units):
+        rows = sample_rows(w.n, int(lengths[bi]), rng)
+        ref, _, _ = orc.unit_rows(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                  w.share_mode, bi, hi, rows)
+        got = host64(O[bi, hi][torch.from_numpy(rows).to(DEV)])
+        check(got, ref, w.dtype, f"{w.name} unit ({bi},{hi})")

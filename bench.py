@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import io
 import json
 import os
@@ -42,7 +43,7 @@ from rank_linear_complexity_gb300.workloads import HEADLINE, WORKLOADS, workload
 
 METRIC = "Linformer attn fwd Mtokens/s at n=4096,k=256 bf16; % of HBM/TC roofline"
 UNIT = "Mtokens/s"
-L2_BYTES = 129 * 2 ** 20
+L2_BYTES = 129e6
 
 
 def load_peaks():
@@ -228,6 +229,8 @@ def run_ours(args):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.workload] if args.workload is not None else HEADLINE
+    if args.batch:
+        w = dataclasses.replace(w, b=args.batch, name=f"{w.name}_b{args.batch}")
     x = workload_inputs(w)
     g = {kk: (v.to(dev) if v is not None else None) for kk, v in x.items()}
     out_dt = torch.bfloat16 if w.dtype == 1 else torch.float32
@@ -374,6 +377,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=None,
                     help="index into the workload table (default: the n=4096, k=256 case)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch size (smaller cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-units", type=int, default=48,
                     help="units of the workload the CPU-baseline oracle pass covers")

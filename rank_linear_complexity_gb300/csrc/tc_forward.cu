@@ -1,10 +1,193 @@
-// Tensor-core (tcgen05 / TMA) path: not wired yet.
+// Host side of the tensor-core path: TMA descriptors, split-n chunking, the
+// stream-ordered workspace and the two launches (projection, then attention).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
 #include "internal.cuh"
+#include "tc_common.cuh"
 
 namespace linformer {
 
-bool tc_supported(int, int, int, int) { return false; }
+bool tc_supported(int n, int d, int k, int dtype) {
+    return dtype != LINFORMER_F32 && d == tc::kD && k >= 1 && k <= tc::kMaxK && n % 8 == 0 &&
+           n <= (1 << 30);
+}
 
-int tc_forward(const Problem &, float *, float *) { return LINFORMER_ERR_UNSUPPORTED; }
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+constexpr int kMaxDev = 64;
+int g_sms[kMaxDev] = {};
+
+int sm_count() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDev) return 148;
+    if (!g_sms[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        g_sms[dev] = v > 0 ? v : 148;
+    }
+    return g_sms[dev];
+}
+
+// 3-D tiled map, 128-byte swizzle, out-of-range elements read as zero.
+bool encode3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t elem,
+              uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * elem, d0 * d1 * elem};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Number of sequence chunks per unit for the projection: the fewest "waves" of
+// equal chunks over the resident CTA slots, with a fixed per-chunk overhead.
+int choose_chunks(int n, int64_t units, int slots, bool ragged) {
+    const int max_c = std::max(1, (n + 255) / 256);
+    int best_c = 1;
+    double best = 1e300;
+    for (int c = 1; c <= std::min(max_c, 64); ++c) {
+        const int ch = ((n + c - 1) / c + tc::kBK - 1) / tc::kBK * tc::kBK;
+        const int c2 = (n + ch - 1) / ch;
+        const double waves = std::ceil((double)units * c2 / slots);
+        double cost = waves * (ch + 256.0);
+        if (ragged) cost *= (ch > 2048 ? 1.25 : 1.0);  // unknown lengths: favour balance
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_c = c2;
+        }
+    }
+    return best_c;
+}
+
+}  // namespace
+
+int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
+    using namespace tc;
+    if (!encoder()) return LINFORMER_ERR_LAUNCH;
+    const int64_t units = p.units();
+    const int kpad = (p.k + 15) / 16 * 16;
+    const int mhalves = (kpad + 127) / 128;
+    const int distinct = p.distinct_f() ? 1 : 0;
+    const int per_head = p.proj_per_head() ? 1 : 0;
+    const size_t stage = (size_t)mhalves * 16384 * (1 + distinct) + 16384;
+    const int stages = (int)std::max<size_t>(2, std::min<size_t>(6, (100 * 1024) / stage));
+    const size_t psmem = project_smem_bytes(mhalves, distinct, stages);
+    const int occ = std::max(1, std::min<int>((int)((228 * 1024) / (psmem + 1024)), 512 / (mhalves * 128)));
+    const int sms = sm_count();
+    const int C = choose_chunks(p.n, units, sms * occ, p.pad != nullptr);
+    const int CH = ((p.n + C - 1) / C + kBK - 1) / kBK * kBK;
+
+    // Workspace: images, split partials, per-unit counters and info words.
+    const size_t img = up256(units * 4 * image_bytes(kpad));
+    const size_t part = C > 1 ? up256((size_t)units * C * kpad * 128 * sizeof(float)) : 0;
+    const size_t cnt = up256(units * sizeof(int));
+    char *ws = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), img + part + 2 * cnt, p.stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return LINFORMER_ERR_ALLOC;
+    }
+    uint8_t *images = reinterpret_cast<uint8_t *>(ws);
+    float *partial = C > 1 ? reinterpret_cast<float *>(ws + img) : nullptr;
+    int *counters = reinterpret_cast<int *>(ws + img + part);
+    int *info = reinterpret_cast<int *>(ws + img + part + cnt);
+    int st = LINFORMER_OK;
+    if (cudaMemsetAsync(counters, 0, cnt, p.stream) != cudaSuccess) st = LINFORMER_ERR_LAUNCH;
+
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t groups = per_head ? (uint64_t)p.h : 1;
+    CUtensorMap tE, tF, tK, tV;
+    if (st == LINFORMER_OK &&
+        !(encode3d(&tE, p.E, bf, 2, p.n, p.k, groups, 64, 128) &&
+          encode3d(&tF, p.f_or_e(), bf, 2, p.n, p.k, groups, 64, 128) &&
+          encode3d(&tK, p.K, bf, 2, kD, p.n, units, 64, kBK) &&
+          encode3d(&tV, p.V, bf, 2, kD, p.n, units, 64, kBK)))
+        st = LINFORMER_ERR_LAUNCH;
+
+    int *status = device_status_ptr();
+    if (st == LINFORMER_OK) {
+        ProjParams pp{};
+        pp.pad = p.pad;
+        pp.partial = partial;
+        pp.images = images;
+        pp.counters = counters;
+        pp.info = info;
+        pp.kbar_out = Kbar_out;
+        pp.vbar_out = Vbar_out;
+        pp.status = status;
+        pp.h = p.h;
+        pp.n = p.n;
+        pp.k = p.k;
+        pp.kpad = kpad;
+        pp.mhalves = mhalves;
+        pp.C = C;
+        pp.CH = CH;
+        pp.stages = stages;
+        pp.distinct = distinct;
+        pp.per_head = per_head;
+        pp.members = per_head ? p.b : (int)units;
+        pp.forced_terms = pv_terms_setting();
+        const int64_t grid = groups * (int64_t)C * pp.members;
+        st = grid > 0x7fffffffLL ? LINFORMER_ERR_SIZE
+                                 : launch_project(tE, tF, tK, tV, pp, (int)grid, psmem, p.stream);
+    }
+
+    if (st == LINFORMER_OK && !Kbar_out) {
+        CUtensorMap tQ, tO;
+        const bool f32out = p.dtype == LINFORMER_BF16_F32OUT;
+        if (!(encode3d(&tQ, p.Q, bf, 2, kD, p.n, units, 64, kTileM) &&
+              (f32out ? encode3d(&tO, p.O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, p.n, units, 32,
+                                 kTileM)
+                      : encode3d(&tO, p.O, bf, 2, kD, p.n, units, 64, kTileM)))) {
+            st = LINFORMER_ERR_LAUNCH;
+        } else {
+            AttnParams ap{};
+            ap.pad = p.pad;
+            ap.images = images;
+            ap.info = info;
+            ap.status = status;
+            ap.h = p.h;
+            ap.n = p.n;
+            ap.k = p.k;
+            ap.kpad = kpad;
+            ap.units = (int)units;
+            ap.tiles_per_unit = (p.n + kTileM - 1) / kTileM;
+            ap.forced_terms = pv_terms_setting();
+            ap.out_fp32 = f32out ? 1 : 0;
+            ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
+            const int64_t tiles = units * ap.tiles_per_unit;
+            const int grid = (int)std::min<int64_t>(sms, tiles);
+            st = launch_attend(tQ, tO, ap, grid, p.stream);
+        }
+    }
+    cudaFreeAsync(ws, p.stream);
+    return st;
+}
 
 }  // namespace linformer

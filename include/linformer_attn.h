@@ -146,6 +146,33 @@ LINFORMER_API int linformer_attn_fwd_host(const void *Q, const void *K, const vo
                             int b, int h, int n, int d, int k,
                             int share_mode, int dtype, void *stream);
 
+/*
+ * linformer_attn_fwd_noalloc: the same operation, arguments and device buffers as
+ * linformer_attn_fwd, for callers that must not allocate device memory while they
+ * run it -- for example a server that reserved its whole memory budget at start-up,
+ * a plugin whose host framework owns every device allocation, code called from an
+ * allocator or out-of-memory handler, or a setup without stream-ordered memory
+ * pools.  It allocates nothing: its workspace is one fixed 32 MiB array in device
+ * memory that every GPU loading this library holds until the process exits.
+ *   - Problems whose workspace does not fit in 32 MiB even without splitting the
+ *     sequence (about b*h*k_pad*512 bytes, k_pad = k rounded up to 16) return
+ *     LINFORMER_ERR_SIZE before anything is launched.
+ *   - Only tensor-core configurations (bf16 inputs, d = 64, k <= 256, n % 8 == 0)
+ *     are served; others return LINFORMER_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the array's address on that device;
+ *     make it before any stream capture starts.
+ *   - Every call reuses the same array and clears its per-unit counters itself;
+ *     calls that overlap on the GPU (other streams, other host threads) race on
+ *     the array and must be serialised by the caller.
+ * The pages describe no counterpart: this is a deployment variant, not part of the
+ * method.
+ */
+LINFORMER_API int linformer_attn_fwd_noalloc(const void *Q, const void *K, const void *V,
+                                             const void *E, const void *F,
+                                             const int32_t *pad_lengths, void *O,
+                                             int b, int h, int n, int d, int k,
+                                             int share_mode, int dtype, void *stream);
+
 /* Which path (linformer_path_kind) a call with these arguments takes, or a
  * negative status if the arguments are invalid.  Host only; launches nothing. */
 LINFORMER_API int linformer_select_path(int b, int h, int n, int d, int k, int share_mode, int dtype);

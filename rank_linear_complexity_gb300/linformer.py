@@ -29,7 +29,7 @@ SYMBOLS = [
     "linformer_attn_fwd", "linformer_project_fwd", "linformer_attn_fwd_host",
     "linformer_select_path", "linformer_status_string", "linformer_debug_read_device_status",
     "linformer_set_pv_terms", "linformer_launch_count", "linformer_profile_enable",
-    "linformer_profile_collect", "linformer_kernel_name",
+    "linformer_profile_collect", "linformer_kernel_name", "linformer_attn_fwd_noalloc",
 ]
 
 
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
             L.linformer_attn_fwd.restype = _i
             L.linformer_attn_fwd_host.argtypes = fwd_args
             L.linformer_attn_fwd_host.restype = _i
+            L.linformer_attn_fwd_noalloc.argtypes = fwd_args
+            L.linformer_attn_fwd_noalloc.restype = _i
             L.linformer_project_fwd.argtypes = [_vp] * 5 + [_vp, _vp] + [_i] * 7 + [_vp]
             L.linformer_project_fwd.restype = _i
             L.linformer_select_path.argtypes = [_i] * 7
@@ -119,6 +121,14 @@ def linformer_attn_fwd_host(Q, K, V, E, F, pad_lengths, O, b, h, n, d, k, share_
     return lib().linformer_attn_fwd_host(_ptr(Q), _ptr(K), _ptr(V), _ptr(E), _ptr(F),
                                          _ptr(pad_lengths), _ptr(O), b, h, n, d, k,
                                          share_mode, dtype, _stream_handle(stream))
+
+
+def linformer_attn_fwd_noalloc(Q, K, V, E, F, pad_lengths, O, b, h, n, d, k, share_mode,
+                               dtype, stream=None) -> int:
+    """Same as linformer_attn_fwd, with the library's fixed device workspace (no allocation)."""
+    return lib().linformer_attn_fwd_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(E), _ptr(F),
+                                            _ptr(pad_lengths), _ptr(O), b, h, n, d, k,
+                                            share_mode, dtype, _stream_handle(stream))
 
 
 def linformer_select_path(b, h, n, d, k, share_mode, dtype) -> int:

@@ -157,6 +157,11 @@ def max_over_ranks(value: float, world: int) -> float:
     return float(t.item())
 
 
+def aggregate_throughput(tokens_per_rank: int, ms_per_step_max: float, world: int) -> float:
+    """Whole-job Mtokens/s: every rank's tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step_max * 1e-3) / 1e6
+
+
 def oracle_sample(w, x, units: int, nthreads: int = 0):
     """Time the oracle on the first `units` units (batch-major); returns
     (seconds, tokens, threads used)."""
@@ -267,7 +272,7 @@ def run_ours(args):
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
     clocks = sampler.stop()
     ms_step = ms_total / args.steps
-    value = world * w.tokens / (ms_step * 1e-3) / 1e6
+    value = aggregate_throughput(w.tokens, ms_step, world)
 
     # --- per-kernel durations: a second pass of K steps with library events -----------
     lf.linformer_profile_enable(True)

@@ -137,8 +137,6 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     const size_t stage = (size_t)mhalves * 16384 * (1 + distinct) + 16384;
     const int stages = (int)std::max<size_t>(2, std::min<size_t>(6, (100 * 1024) / stage));
     const size_t psmem = project_smem_bytes(mhalves, distinct, stages);
-    const int occ = std::max(1, std::min<int>((int)((228 * 1024) / (psmem + 1024)),
-                                              512 / (mhalves * 128)));
     // Fewest waves of equal chunks over the resident CTA slots, among the chunk
     // counts whose fp32 partials still fit next to the images.
     int C = 1;
@@ -146,17 +144,17 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     for (int c = 1; c <= std::min(64, std::max(1, (n + 255) / 256)); ++c) {
         const int ch = ((n + c - 1) / c + kBK - 1) / kBK * kBK;
         const int c2 = (n + ch - 1) / ch;
-        const size_t part = c2 > 1 ? round256((size_t)units * c2 * kpad * 128 * sizeof(float)) : 0;
+        const size_t part = round256(partial_bytes(units, c2, mhalves));
         if (img + part + 2 * cnt > kScratchBytes) continue;
-        double cost = std::ceil((double)units * c2 / (sms * occ)) * (ch + 256.0);
-        if (pad_lengths && ch > 2048) cost *= 1.25;
+        double cost = (double)((units * c2 + sms - 1) / sms) * (ch + 192.0) + (c2 > 1 ? 512.0 : 0.0);
+        if (pad_lengths && ch > 2048) cost *= 1.3;
         if (cost < best - 1e-9) {
             best = cost;
             C = c2;
         }
     }
     const int CH = ((n + C - 1) / C + kBK - 1) / kBK * kBK;
-    const size_t part = C > 1 ? round256((size_t)units * C * kpad * 128 * sizeof(float)) : 0;
+    const size_t part = round256(partial_bytes(units, C, mhalves));
     uint8_t *images = scratch;
     float *partial = C > 1 ? reinterpret_cast<float *>(scratch + img) : nullptr;
     int *counters = reinterpret_cast<int *>(scratch + img + part);

@@ -32,9 +32,37 @@ __host__ __device__ inline int info_exp(int info) { return (info >> 8) & 0xff; }
 // 2^-11 * max|Vbar| <= 0.0117 at 24 -- together under the 2e-2 absolute bar.
 constexpr float kOneTermMaxV = 24.0f;
 
+// Split-n partial sums: per (unit, chunk, 128-row half of k_pad) one contiguous
+// 64 KB block [128 columns][128 rows] fp32 (columns 0-63 Kbar, 64-127 Vbar), so
+// that each 64-column half is one 32 KB slice for a single bulk copy.
+__host__ __device__ inline size_t partial_bytes(int64_t units, int C, int mhalves) {
+    return C > 1 ? (size_t)units * C * mhalves * 128 * 128 * sizeof(float) : 0;
+}
+
+// Fewest rows per SM: equal chunks of the sequence spread over the SMs, plus a
+// per-CTA and a split cost (in row-equivalents); unknown ragged lengths favour
+// chunks of at most 2048 rows.
+inline int choose_chunks(int n, int64_t units, int sms, bool ragged) {
+    const int max_c = n / 256 > 1 ? n / 256 : 1;
+    int best_c = 1;
+    double best = 1e300;
+    for (int c = 1; c <= (max_c < 64 ? max_c : 64); ++c) {
+        const int ch = ((n + c - 1) / c + kBK - 1) / kBK * kBK;
+        const int c2 = (n + ch - 1) / ch;
+        const double per_sm = (double)((units * c2 + sms - 1) / sms);
+        double cost = per_sm * (ch + 192.0) + (c2 > 1 ? 512.0 : 0.0);
+        if (ragged && ch > 2048) cost *= 1.3;
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_c = c2;
+        }
+    }
+    return best_c;
+}
+
 struct ProjParams {
     const int32_t *pad;
-    float *partial;      // [units][C][kpad][128] fp32 (used when C > 1)
+    float *partial;      // see partial_bytes (used when C > 1)
     uint8_t *images;     // [units][4][kpad * 128 bytes]
     int *counters;       // [units], zero on entry, left zero on exit
     int *info;           // [units]

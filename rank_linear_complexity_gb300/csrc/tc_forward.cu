@@ -65,26 +65,6 @@ bool encode3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, size_t e
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Number of sequence chunks per unit for the projection: the fewest "waves" of
-// equal chunks over the resident CTA slots, with a fixed per-chunk overhead.
-int choose_chunks(int n, int64_t units, int slots, bool ragged) {
-    const int max_c = std::max(1, (n + 255) / 256);
-    int best_c = 1;
-    double best = 1e300;
-    for (int c = 1; c <= std::min(max_c, 64); ++c) {
-        const int ch = ((n + c - 1) / c + tc::kBK - 1) / tc::kBK * tc::kBK;
-        const int c2 = (n + ch - 1) / ch;
-        const double waves = std::ceil((double)units * c2 / slots);
-        double cost = waves * (ch + 256.0);
-        if (ragged) cost *= (ch > 2048 ? 1.25 : 1.0);  // unknown lengths: favour balance
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_c = c2;
-        }
-    }
-    return best_c;
-}
-
 }  // namespace
 
 int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
@@ -98,14 +78,13 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
     const size_t stage = (size_t)mhalves * 16384 * (1 + distinct) + 16384;
     const int stages = (int)std::max<size_t>(2, std::min<size_t>(6, (100 * 1024) / stage));
     const size_t psmem = project_smem_bytes(mhalves, distinct, stages);
-    const int occ = std::max(1, std::min<int>((int)((228 * 1024) / (psmem + 1024)), 512 / (mhalves * 128)));
     const int sms = sm_count();
-    const int C = choose_chunks(p.n, units, sms * occ, p.pad != nullptr);
+    const int C = tc::choose_chunks(p.n, units, sms, p.pad != nullptr);
     const int CH = ((p.n + C - 1) / C + kBK - 1) / kBK * kBK;
 
     // Workspace: images, split partials, per-unit counters and info words.
     const size_t img = up256(units * 4 * image_bytes(kpad));
-    const size_t part = C > 1 ? up256((size_t)units * C * kpad * 128 * sizeof(float)) : 0;
+    const size_t part = up256(partial_bytes(units, C, mhalves));
     const size_t cnt = up256(units * sizeof(int));
     char *ws = nullptr;
     if (cudaMallocAsync(reinterpret_cast<void **>(&ws), img + part + 2 * cnt, p.stream) !=

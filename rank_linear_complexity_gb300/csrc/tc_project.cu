@@ -13,8 +13,9 @@
 //
 // Chunks of the same unit are summed in a fixed order (chunk 0, 1, ...) by
 // whichever CTA of the unit arrives last, so the result does not depend on
-// scheduling.  That CTA converts to the split images the attention step reads
-// and picks the number of P.Vbar products from max|Vbar|.
+// scheduling.  That CTA pulls the other chunks' sums in as 32 KB slices by bulk
+// copy, converts to the split images the attention step reads and picks the
+// number of P.Vbar products from max|Vbar|.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -29,7 +30,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 128;
-constexpr int kVsStride = 65;  // fp32 scratch row stride (conflict-free per-row access)
+constexpr int kSlice = 64 * 128;  // floats in one 64-column half of a 128-row block
 
 __device__ __forceinline__ int valid_length(const int32_t *pad, int batch, int n) {
     if (!pad) return n;
@@ -84,7 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    uint64_t *fin = acc_full + 1;  // two slice buffers of the split reduction
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 2);
     float *red = reinterpret_cast<float *>(tmem_slot + 4);
@@ -96,6 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(empty + s, 1);
         }
         mbar_init(acc_full, 1);
+        mbar_init(fin, 1);
+        mbar_init(fin + 1, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_mbar_init();
@@ -115,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // ---------------- TMA producer
+            int issued = 0;
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % S;
                 if (it >= S && !mbar_wait(empty + s, ((it / S) - 1) & 1, p.status, 11, abort_flag))
@@ -130,42 +135,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *bk = st + a_bytes * (1 + p.distinct);
                 tma_load_3d(bk, &tK, full + s, 0, x, u);
                 tma_load_3d(bk + 8192, &tV, full + s, 0, x, u);
+                issued = it + 1;
             }
-            // Let every copy this thread started land before the CTA may exit.
-            const int first = nkb > S ? nkb - S : 0;
-            for (int it = first; it < nkb; ++it)
-                mbar_wait(full + (it % S), (it / S) & 1, p.status, 12, abort_flag);
+            // Let every copy this thread started land before the CTA may exit
+            // (also after an abort: a copy must not outlive the CTA).
+            for (int it = issued > S ? issued - S : 0; it < issued; ++it)
+                mbar_wait_drain(full + (it % S), (it / S) & 1);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {  // ---------------- MMA issuer
-            const uint32_t idesc128 = idesc_f16(128, 128, 1, 0, 1);
-            const uint32_t idesc64 = idesc_f16(128, 64, 1, 0, 1);
-            bool ok = true;
-            for (int it = 0; it < nkb && ok; ++it) {
-                const int s = it % S;
-                if (!mbar_wait(full + s, (it / S) & 1, p.status, 13, abort_flag)) {
-                    ok = false;
-                    break;
+    } else if (warp == 1) {  // ---------------- MMA warp (lane 0 issues, all lanes zero)
+        const uint32_t idesc128 = idesc_f16(128, 128, 1, 0, 1);
+        const uint32_t idesc64 = idesc_f16(128, 64, 1, 0, 1);
+        bool ok = true;
+        for (int it = 0; it < nkb && ok; ++it) {
+            const int s = it % S;
+            int got = 1;
+            if (lane == 0) got = mbar_wait(full + s, (it / S) & 1, p.status, 13, abort_flag) ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            __syncwarp();
+            if (!got) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint8_t *st = smem + (size_t)s * stage_bytes;
+            uint8_t *bk = st + a_bytes * (1 + p.distinct);
+            uint8_t *bv = bk + 8192;
+            const int valid = rows - it * kBK;
+            if (valid < kBK) {  // rows past the valid length count as zero
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                for (int e = lane; e < (kBK - valid) * 8; e += 32) {
+                    const int r = valid + (e >> 3), q = e & 7;
+                    reinterpret_cast<uint4 *>(bk + r * kRowBytes)[q] = z;
+                    reinterpret_cast<uint4 *>(bv + r * kRowBytes)[q] = z;
                 }
-                tc_fence_after();
-                uint8_t *st = smem + (size_t)s * stage_bytes;
-                uint8_t *bk = st + a_bytes * (1 + p.distinct);
-                uint8_t *bv = bk + 8192;
-                const int valid = rows - it * kBK;
-                if (valid < kBK) {  // rows past the valid length count as zero
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-                    for (int r = valid; r < kBK; ++r) {
-                        uint4 *rk = reinterpret_cast<uint4 *>(bk + r * kRowBytes);
-                        uint4 *rv = reinterpret_cast<uint4 *>(bv + r * kRowBytes);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            rk[q] = z;
-                            rv[q] = z;
-                        }
-                    }
-                    fence_proxy_async_smem();
-                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) {
                 const uint32_t a0 = smem_u32(st), f0 = smem_u32(st + a_bytes);
                 const uint32_t k0 = smem_u32(bk), v0 = smem_u32(bv);
 #pragma unroll
@@ -189,6 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(empty + s);
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             if (ok && nkb > 0)
                 mma_commit(acc_full);
             else
@@ -204,27 +214,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool aborted = *abort_flag != 0;
     const int jl = warp * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const size_t part_unit = (size_t)p.kpad * 128;  // floats per (unit, chunk) partial
 
     if (!aborted && Cu > 1) {
-        // Partial layout [unit][chunk][column][row]: a warp stores 32 consecutive floats.
-        float *mine = p.partial + ((size_t)u * p.C + c) * part_unit;
+        // This chunk's sums, [half of k_pad][column][row]: a warp stores 128 contiguous bytes.
+        float *mine = p.partial + ((size_t)u * p.C + c) * p.mhalves * 2 * kSlice;
+#pragma unroll 1
         for (int mh = 0; mh < p.mhalves; ++mh) {
-            const int j = mh * 128 + jl;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t v[32];
-                if (nkb) {
-                    tmem_ld32(lane_base + mh * 128 + cc * 32, v);
-                } else {
+                tmem_ld32(lane_base + mh * 128 + cc * 32, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;
-                }
-                if (j < p.kpad) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        mine[(size_t)(cc * 32 + i) * p.kpad + j] = __uint_as_float(v[i]);
-                }
+                for (int i = 0; i < 32; ++i)
+                    mine[(size_t)mh * 2 * kSlice + (cc * 32 + i) * 128 + jl] = __uint_as_float(v[i]);
             }
         }
         __threadfence();
@@ -235,68 +237,106 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (!aborted && (Cu == 1 || *last_flag)) {
         __threadfence();
-        float *vs = reinterpret_cast<float *>(smem);  // [kpad][65] fp32 Vbar sums (stages are idle)
+        // The other chunks' sums come in as 32 KB slices (one 64-column half of one
+        // 128-row block) by bulk copy into two shared buffers (the stages are idle);
+        // they are added in chunk order 0, 1, ... whatever chunk this CTA owns.
+        float *sbuf = reinterpret_cast<float *>(smem);
+        const int per = Cu - 1;
+        const int nslices = p.mhalves * 2 * per;
+        auto slice_src = [&](int idx) {
+            const int mh = idx / (2 * per), rem = idx % (2 * per);
+            const int half = rem / per, k2 = rem % per;
+            const int c2 = k2 < c ? k2 : k2 + 1;
+            return p.partial + (((size_t)u * p.C + c2) * p.mhalves + mh) * 2 * kSlice + half * kSlice;
+        };
+        int sl_issued = 0;  // slice copies started (thread 0's count)
+        if (tid == 0 && nslices > 0) {
+            fence_proxy_async_global();
+            for (int i = 0; i < 2 && i < nslices; ++i, ++sl_issued) {
+                mbar_arrive_expect_tx(fin + i, kSlice * 4);
+                bulk_load(sbuf + i * kSlice, slice_src(i), kSlice * 4, fin + i);
+            }
+        }
         uint8_t *img = p.images + (size_t)u * 4 * image_bytes(p.kpad);
+        int sidx = 0;
         float vmax = 0.f;
+        bool ok = true;
+#pragma unroll 1
         for (int mh = 0; mh < p.mhalves; ++mh) {
             const int j = mh * 128 + jl;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                float acc[32];
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t tcol = lane_base + mh * 128 + half * 64;
+                float acc[64];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-                for (int c2 = 0; c2 < Cu; ++c2) {  // fixed order: chunk 0, 1, ...
+                for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+#pragma unroll 1
+                for (int c2 = 0; c2 < Cu; ++c2) {
                     if (c2 == c) {
                         if (nkb) {
-                            uint32_t v[32];
-                            tmem_ld32(lane_base + mh * 128 + cc * 32, v);
+                            uint32_t v[64];
+                            tmem_ld64(tcol, v);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(v[i]);
+                            for (int i = 0; i < 64; ++i) acc[i] += __uint_as_float(v[i]);
                         }
-                    } else if (j < p.kpad) {
-                        const float *src = p.partial + ((size_t)u * p.C + c2) * part_unit;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[i] += __ldcg(src + (size_t)(cc * 32 + i) * p.kpad + j);
+                        continue;
                     }
+                    const int b = sidx & 1;
+                    if (!mbar_wait(fin + b, (sidx >> 1) & 1, p.status, 15, abort_flag)) ok = false;
+                    const float *sb = sbuf + b * kSlice;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) acc[i] += sb[i * 128 + jl];
+                    __syncthreads();
+                    if (tid == 0 && ok && sidx + 2 < nslices) {
+                        mbar_arrive_expect_tx(fin + b, kSlice * 4);
+                        bulk_load(sbuf + b * kSlice, slice_src(sidx + 2), kSlice * 4, fin + b);
+                        ++sl_issued;
+                    }
+                    ++sidx;
                 }
-                if (j >= p.kpad) continue;
                 if (j >= p.k) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
                 }
-                if (cc < 2) {  // Kbar: bf16 hi + bf16 lo
+                if (half == 0) {  // Kbar: bf16 hi + bf16 lo images
+                    if (j < p.kpad) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t hi[4], lo[4];
+                        for (int q = 0; q < 8; ++q) {
+                            uint32_t hi[4], lo[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x0 = acc[q4 * 8 + 2 * e], x1 = acc[q4 * 8 + 2 * e + 1];
-                            const __nv_bfloat16 h0 = __float2bfloat16_rn(x0);
-                            const __nv_bfloat16 h1 = __float2bfloat16_rn(x1);
-                            hi[e] = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-                            lo[e] = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
-                            if (p.kbar_out && j < p.k) {
-                                const __nv_bfloat162 l2 = *reinterpret_cast<__nv_bfloat162 *>(&lo[e]);
-                                float *o = p.kbar_out + ((size_t)u * p.k + j) * kD + cc * 32 + q4 * 8 + 2 * e;
-                                o[0] = __bfloat162float(h0) + __bfloat162float(l2.x);
-                                o[1] = __bfloat162float(h1) + __bfloat162float(l2.y);
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 = acc[q * 8 + 2 * e], x1 = acc[q * 8 + 2 * e + 1];
+                                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0);
+                                const __nv_bfloat16 h1 = __float2bfloat16_rn(x1);
+                                const float r0 = x0 - __bfloat162float(h0), r1 = x1 - __bfloat162float(h1);
+                                hi[e] = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                                lo[e] = pack_bf16(r0, r1);
+                                if (p.kbar_out && j < p.k) {
+                                    float *o = p.kbar_out + ((size_t)u * p.k + j) * kD + q * 8 + 2 * e;
+                                    o[0] = __bfloat162float(h0) + __bfloat162float(__float2bfloat16_rn(r0));
+                                    o[1] = __bfloat162float(h1) + __bfloat162float(__float2bfloat16_rn(r1));
+                                }
                             }
+                            *image_chunk(img, j, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *image_chunk(img + image_bytes(p.kpad), j, q) =
+                                make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         }
-                        const int q = cc * 4 + q4;
-                        *image_chunk(img, j, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *image_chunk(img + image_bytes(p.kpad), j, q) =
-                            make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
-                } else {  // Vbar: keep fp32 until the unit's magnitude is known
+                } else {  // Vbar: park the fp32 sums in TMEM until max|Vbar| is known
+                    uint32_t w0[32], w1[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        vs[j * kVsStride + (cc - 2) * 32 + i] = acc[i];
-                        vmax = fmaxf(vmax, fabsf(acc[i]));
+                        w0[i] = __float_as_uint(acc[i]);
+                        w1[i] = __float_as_uint(acc[32 + i]);
+                        vmax = fmaxf(vmax, fmaxf(fabsf(acc[i]), fabsf(acc[32 + i])));
                     }
+                    tmem_st32(tcol, w0);
+                    tmem_st32(tcol + 32, w1);
                 }
             }
         }
+        if (tid == 0)  // copies that were started but not consumed (only after an abort)
+            for (int i = sidx; i < sl_issued; ++i) mbar_wait_drain(fin + (i & 1), (i >> 1) & 1);
         // Unit-wide max|Vbar| -> scale exponent and number of P.Vbar products.
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
@@ -307,24 +347,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (e < 100 && vmax * exp2f(-(float)e) >= 16384.f) ++e;
         const float vscale = exp2f(-(float)e);
         const int terms = p.forced_terms ? p.forced_terms : (vmax < kOneTermMaxV ? 1 : 3);
+#pragma unroll 1
         for (int mh = 0; mh < p.mhalves; ++mh) {
             const int j = mh * 128 + jl;
+            uint32_t v[64];
+            tmem_ld64(lane_base + mh * 128 + 64, v);
             if (j >= p.kpad) continue;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
-                    const float x0 = vs[j * kVsStride + q * 8 + 2 * e2] * vscale;
-                    const float x1 = vs[j * kVsStride + q * 8 + 2 * e2 + 1] * vscale;
+                    const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
+                    const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
                     const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                    const float r0 = x0 - __half2float(h0), r1 = x1 - __half2float(h1);
                     hi[e2] = pack_f16(__half2float(h0), __half2float(h1));
-                    lo[e2] = pack_f16(x0 - __half2float(h0), x1 - __half2float(h1));
+                    lo[e2] = pack_f16(r0, r1);
                     if (p.vbar_out && j < p.k) {
-                        const __half2 l2 = *reinterpret_cast<__half2 *>(&lo[e2]);
                         float *o = p.vbar_out + ((size_t)u * p.k + j) * kD + q * 8 + 2 * e2;
-                        o[0] = (__half2float(h0) + __half2float(l2.x)) / vscale;
-                        o[1] = (__half2float(h1) + __half2float(l2.y)) / vscale;
+                        o[0] = (__half2float(h0) + __half2float(__float2half_rn(r0))) / vscale;
+                        o[1] = (__half2float(h1) + __half2float(__float2half_rn(r1))) / vscale;
                     }
                 }
                 *image_chunk(img + 2 * image_bytes(p.kpad), j, q) =
@@ -333,12 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
-        if (tid == 0) {
+        if (tid == 0 && ok) {
             p.info[u] = pack_info(terms, e);
             p.counters[u] = 0;
         }
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 

@@ -5,26 +5,40 @@
 // query rows produce zero output, section Model, padding paragraph).
 //
 // Persistent CTAs walk a contiguous range of 128-row query tiles (unit-major).
-// Roles (320 threads):
-//   warps 0-3  softmax/epilogue group 0, warps 4-7 group 1: tiles of the range
-//              alternate between the groups (ping-pong), one query row per
-//              thread (TMEM lane = row);
-//   warp 8     producer: Q per tile by TMA into a ring, and the projection
-//              step's pre-swizzled images (Kbar hi/lo bf16, Vbar hi[/lo] fp16)
-//              once per unit by bulk copy;
-//   warp 9     MMA issuer (one thread), one tile of look-ahead so that the
-//              scores of the next tile are computed while a group is busy with
-//              the softmax of the current one.
-// TMEM (512 columns) holds two 256-column buffers, one per group.  In a buffer:
-//   S  = Q . Kbar_hi^T + Q . Kbar_lo^T   fp32, columns [0, k_pad)
-//   P  (fp16, packed two per column)     over the consumed S columns [0, k_pad/2)
-//   O  = P . Vbar_hi                     fp32, columns [128, 192)
+// The tiles that hold query rows (the non-empty ones) alternate between two
+// 256-column TMEM buffers; tile j of the range uses buffer j % 2.
+//
+// Each tile's key columns are cut into two halves (a: columns [0, c_b),
+// b: [c_b, k)).  Roles (512 threads):
+//   warps 0-7   softmax: warp w takes TMEM lane quarter w % 4 and key half
+//               w / 4 of every tile, so one query row is shared by two
+//               threads that swap their partial maxima through shared memory;
+//               each writes its P half (fp16, packed two per column) over
+//               the scores it has read and its partial row sum to shared
+//               memory;
+//   warps 8-11  epilogue, every tile in order: O = O_a + O_b out of TMEM
+//               (which frees the buffer), scaled by 2^e / row sum, rounded,
+//               staged with the 128-byte swizzle and stored by TMA in 16 KB
+//               pieces; tiles past the valid length are written as zeros;
+//   warp 12     producer: Q per tile by TMA into a ring, and per unit the
+//               projection step's pre-swizzled Kbar hi/lo images by bulk copy,
+//               as soon as the previous unit's score products have finished;
+//   warp 13     one thread issues the score products of each tile once its
+//               buffer is free;
+//   warps 14-15 one thread each issues P.V of one key half once the tile's P
+//               is ready, into its own accumulator O_a / O_b; warp 14 also
+//               loads the unit's Vbar image(s) after the previous unit's P.V.
+// A single thread issues at most about one MMA per 70-80 cycles whatever its
+// shape, so P.V (16 MMAs of N = 64 per tile) is spread over two threads.
+// In a buffer (256 columns), with c_b = 128 when k_pad > 128:
+//   S   = Q . Kbar_hi^T + Q . Kbar_lo^T   fp32, columns [0, k_pad)
+//   P_a over S columns [0, c_b / 2), P_b over [c_b, c_b + (k_pad - c_b) / 2)
+//   O_a = P_a . Vbar_a at column 64 (128 when k_pad <= 128), O_b at column 192
 // Units whose |Vbar| is large take three products for P . Vbar (P_lo . Vbar_hi
-// and P_hi . Vbar_lo added); such a tile also uses the other group's buffer
-// (P_lo at its column 0, O at its column 128) and runs without look-ahead.
+// and P_hi . Vbar_lo added); P_lo then sits in the other buffer at the same
+// columns as P, so such a tile holds both buffers and runs alone.
 // The softmax is exact and two-pass (row max, then exp2 with the 1/sqrt(d)
-// scale folded in, row sum).  The epilogue scales by 2^e / sum, rounds, stages
-// a 128-byte-swizzled tile and TMA-stores it; scores never leave the SM.
+// scale folded in, row sum); scores never leave the SM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -38,12 +52,14 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr uint32_t kBufCols = 256, kColO = 128, kTmemCols = 512;
-constexpr uint32_t kImg = 32768;  // largest image: 256 rows x 128 bytes
+constexpr int kThreads = 512;
+constexpr int kEpilogueWarp = 8, kProducerWarp = 12, kQkWarp = 13, kPvWarp = 14;
+constexpr uint32_t kBufCols = 256, kTmemCols = 512;
+constexpr uint32_t kImg = 32768;    // largest image: 256 rows x 128 bytes
 constexpr uint32_t kQBytes = 16384;
-constexpr int kMaxQSlots = 4;     // Q ring depth with bf16 output (2 with fp32 output)
+constexpr int kQSlots = 3;
+constexpr uint32_t kPiece = 16384;  // one staged store: 128 rows x 128 bytes
+constexpr uint32_t kEpilogueBarrier = 1, kSoftmaxBarrier = 2;
 
 __device__ __forceinline__ int valid_length(const int32_t *pad, int batch, int n) {
     if (!pad) return n;
@@ -70,78 +86,200 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *s
     return ok != 0;
 }
 
-// One 32-column chunk of the second softmax pass: p = 2^(s * scale - mb) for the
-// valid columns (MASKED: columns >= k are set to zero), written back as packed
-// fp16 over S columns [cc/2, cc/2 + 16) (all already read).  One product keeps
-// the row sum of the rounded values; three products keep P_lo = fp16(p - P_hi)
-// in the other buffer and sum p itself.
-template <int TERMS, bool MASKED>
-__device__ __forceinline__ void softmax_chunk(uint32_t buf, uint32_t other, int cc, int k,
-                                              float scale, float mb, float &l0, float &l1) {
-    uint32_t v[32];
-    tmem_ld32(buf + cc, v);
-    uint32_t ph[16], pl[16];
-    const float2 sc = make_float2(scale, scale), nb = make_float2(-mb, -mb);
+// Split of a tile's key columns between the two softmax halves.
+struct KeySplit {
+    int cb;      // first column of half b
+    int n0, n1;  // 32-column chunks per half (the last chunk may be ragged)
+    int s0, s1;  // 16-key MMA steps per half
+    int oa, ob;  // TMEM columns of O_a, O_b within a buffer
+};
+__device__ __forceinline__ KeySplit key_split(int k, int kpad) {
+    const int nch = (k + 31) >> 5;
+    KeySplit s;
+    if (kpad > 128) {
+        s.n0 = 4;
+        s.cb = 128;
+        s.oa = 64;  // the second half of half a's S columns, consumed by then
+    } else {
+        s.n0 = (nch + 1) >> 1;
+        s.cb = 32 * s.n0;
+        s.oa = 128;
+    }
+    s.n1 = nch - s.n0;
+    s.ob = 192;
+    s.s0 = (s.cb < kpad ? s.cb : kpad) >> 4;
+    s.s1 = s.n1 > 0 ? (kpad - s.cb) >> 4 : 0;
+    return s;
+}
+
+// Walks a CTA's contiguous range of tiles [begin, end) in unit-major order with
+// the unit, tile, valid length and product count kept up to date incrementally
+// (no per-tile 64-bit division, no per-tile global loads).
+struct TileWalk {
+    long long T, end;
+    int u, t, L, terms;
+    __device__ __forceinline__ TileWalk(const AttnParams &p, long long b, long long e)
+        : T(b), end(e), u(0), t(0), L(0), terms(1) {
+        if (T < end) {
+            u = (int)(T / p.tiles_per_unit);
+            t = (int)(T % p.tiles_per_unit);
+            load_unit(p);
+        }
+    }
+    __device__ __forceinline__ void load_unit(const AttnParams &p) {
+        L = valid_length(p.pad, u / p.h, p.n);
+        terms = p.forced_terms ? p.forced_terms : info_terms(__ldg(p.info + u));
+    }
+    __device__ __forceinline__ bool more() const { return T < end; }
+    __device__ __forceinline__ bool live() const { return t * kTileM < L; }
+    __device__ __forceinline__ void next(const AttnParams &p) {
+        ++T;
+        if (++t == p.tiles_per_unit) {
+            t = 0;
+            ++u;
+            if (T < end) load_unit(p);  // never past the last unit of the range
+        }
+    }
+};
+
+// Running row max over one 32-column chunk (MASKED: columns >= k are ignored).
+template <bool MASKED>
+__device__ __forceinline__ void max_chunk(const uint32_t (&v)[32], int c0, int k, float &m0,
+                                          float &m1, float &m2, float &m3) {
+    if (MASKED) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            if (c0 + i < k) m0 = fmaxf(m0, __uint_as_float(v[i]));
+            if (c0 + i + 1 < k) m1 = fmaxf(m1, __uint_as_float(v[i + 1]));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+            m0 = max3(m0, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+            m1 = max3(m1, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+            m2 = max3(m2, __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+            m3 = max3(m3, __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
+        }
+    }
+}
+
+// Second-pass work on one 32-column chunk at column c0: p = 2^(s * scale - mb)
+// (MASKED: columns >= k give zero), written as packed fp16 to the 16 columns
+// at pcol (already read).  The row sum adds p in fp32.
+template <bool MASKED>
+__device__ __forceinline__ void exp_chunk(const uint32_t (&v)[32], uint32_t pcol, int c0, int k,
+                                          float scale, float mb, float &l0, float &l1) {
+    uint32_t ph[16];
+    const float nb = -mb;
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-        const float2 x = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc, nb);
-        float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+        float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * e]), scale, nb));
+        float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), scale, nb));
         if (MASKED) {
-            if (cc + 2 * e >= k) p0 = 0.f;
-            if (cc + 2 * e + 1 >= k) p1 = 0.f;
+            if (c0 + 2 * e >= k) p0 = 0.f;
+            if (c0 + 2 * e + 1 >= k) p1 = 0.f;
         }
-        const __half2 h = __floats2half2_rn(p0, p1);
-        ph[e] = *reinterpret_cast<const uint32_t *>(&h);
-        if (TERMS == 1) {
-            l0 = add_f32_f16(l0, __low2half(h));
-            l1 = add_f32_f16(l1, __high2half(h));
-        } else {
-            const float2 hf = __half22float2(h);
+        ph[e] = pack_f16(p0, p1);
+        l0 += p0;
+        l1 += p1;
+    }
+    tmem_st16_async(pcol, ph);
+}
+
+// The same for three products: P_hi at pcol and P_lo = fp16(p - P_hi) at lcol
+// (the other buffer), the row sum of p in fp32.
+template <bool MASKED>
+__device__ __forceinline__ void exp_chunk3(const uint32_t (&v)[32], uint32_t pcol, uint32_t lcol,
+                                           int c0, int k, float scale, float mb, float &l0,
+                                           float &l1) {
+    const float nb = -mb;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // two halves of 16 columns keep the registers in budget
+        uint32_t ph[8], pl[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int i = 16 * h + 2 * e;
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), scale, nb));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[i + 1]), scale, nb));
+            if (MASKED) {
+                if (c0 + i >= k) p0 = 0.f;
+                if (c0 + i + 1 >= k) p1 = 0.f;
+            }
+            ph[e] = pack_f16(p0, p1);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&ph[e]));
             pl[e] = pack_f16(p0 - hf.x, p1 - hf.y);
             l0 += p0;
             l1 += p1;
         }
+        tmem_st8_async(pcol + 8 * h, ph);
+        tmem_st8_async(lcol + 8 * h, pl);
     }
-    tmem_st16(buf + (cc >> 1), ph);
-    if (TERMS == 3) tmem_st16(other + (cc >> 1), pl);
 }
 
-// Exact two-pass row softmax of one tile row (this thread's TMEM lane); returns
-// the row sum.  P replaces S in `buf` (and P_lo goes to `other` for 3 products).
-template <int TERMS>
-__device__ __forceinline__ float softmax_row(uint32_t buf, uint32_t other, int k, float scale) {
-    const int kfull = k & ~63;  // columns in whole 64-column chunks
-    float m0 = -INFINITY, m1 = -INFINITY;
+// This thread's half of one tile row: chunks [0, nch) starting at column c0 of
+// `buf` (all columns >= k are masked).  The partial max is swapped with the
+// partner thread (the other half of the row) through shared memory; returns the
+// partial row sum.  TMEM loads run one chunk ahead of the arithmetic.
+__device__ __forceinline__ float softmax_half(uint32_t buf, uint32_t other, int c0, int nch,
+                                              int k, float scale, bool three, float *xmine,
+                                              const float *xpartner, bool &ok) {
+    uint32_t va[32], vb[32];
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+    if (!ok) nch = 0;  // this warp's wait failed: skip the work, still meet the others
+    if (nch > 0) tmem_ld32_async(buf + c0, va);
 #pragma unroll 1
-    for (int cc = 0; cc < kfull; cc += 64) {
-        uint32_t v[64];
-        tmem_ld64(buf + cc, v);
-#pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-            m0 = max3(m0, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-            m1 = max3(m1, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+    for (int c = 0; c < nch; c += 2) {
+        const int ca = c0 + 32 * c, cb = ca + 32;
+        tmem_wait_ld(va);
+        if (c + 1 < nch) tmem_ld32_async(buf + cb, vb);
+        if (ca + 32 <= k) max_chunk<false>(va, ca, k, m0, m1, m2, m3);
+        else max_chunk<true>(va, ca, k, m0, m1, m2, m3);
+        if (c + 1 < nch) {
+            tmem_wait_ld(vb);
+            if (c + 2 < nch) tmem_ld32_async(buf + cb + 32, va);
+            if (cb + 32 <= k) max_chunk<false>(vb, cb, k, m0, m1, m2, m3);
+            else max_chunk<true>(vb, cb, k, m0, m1, m2, m3);
         }
     }
-    if (kfull < k) {
-        uint32_t v[64];
-        tmem_ld64(buf + kfull, v);
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-            if (kfull + i < k) m0 = fmaxf(m0, __uint_as_float(v[i]));
-    }
-    const float mb = fmaxf(m0, m1) * scale;
+    const float mpart = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+    *xmine = mpart;
+    ok = named_barrier_and(kSoftmaxBarrier, 256, ok);  // all eight warps, whatever happened
+    if (!ok) return 0.f;
+    const float mb = fmaxf(mpart, *xpartner) * scale;
     float l0 = 0.f, l1 = 0.f;
-    const int k32 = k & ~31;  // columns in whole 32-column chunks
+    if (three) {  // rare; one chunk in registers at a time
 #pragma unroll 1
-    for (int cc = 0; cc < k32; cc += 32)
-        softmax_chunk<TERMS, false>(buf, other, cc, k, scale, mb, l0, l1);
-    if (k32 < k) softmax_chunk<TERMS, true>(buf, other, k32, k, scale, mb, l0, l1);
+        for (int c = 0; c < nch; ++c) {
+            const int ca = c0 + 32 * c;
+            tmem_ld32_async(buf + ca, va);
+            tmem_wait_ld(va);
+            if (ca + 32 <= k)
+                exp_chunk3<false>(va, buf + c0 + 16 * c, other + c0 + 16 * c, ca, k, scale, mb, l0, l1);
+            else
+                exp_chunk3<true>(va, buf + c0 + 16 * c, other + c0 + 16 * c, ca, k, scale, mb, l0, l1);
+        }
+    } else {
+        if (nch > 0) tmem_ld32_async(buf + c0, va);
+#pragma unroll 1
+        for (int c = 0; c < nch; c += 2) {
+            const int ca = c0 + 32 * c, cb = ca + 32;
+            tmem_wait_ld(va);
+            if (c + 1 < nch) tmem_ld32_async(buf + cb, vb);
+            if (ca + 32 <= k) exp_chunk<false>(va, buf + c0 + 16 * c, ca, k, scale, mb, l0, l1);
+            else exp_chunk<true>(va, buf + c0 + 16 * c, ca, k, scale, mb, l0, l1);
+            if (c + 1 < nch) {
+                tmem_wait_ld(vb);
+                if (c + 2 < nch) tmem_ld32_async(buf + cb + 32, va);
+                if (cb + 32 <= k)
+                    exp_chunk<false>(vb, buf + c0 + 16 * (c + 1), cb, k, scale, mb, l0, l1);
+                else
+                    exp_chunk<true>(vb, buf + c0 + 16 * (c + 1), cb, k, scale, mb, l0, l1);
+            }
+        }
+    }
+    tmem_wait_st();
     return l0 + l1;
 }
-
-struct Tile {
-    int u, t, w, terms;
-};
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_attend_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tO,
@@ -149,15 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t stage_o = p.out_fp32 ? 32768u : 16384u;
-    const int QS = p.out_fp32 ? 2 : kMaxQSlots;  // Q ring slots
     uint8_t *sKh = smem, *sKl = smem + kImg, *sVh = smem + 2 * kImg, *sVl = smem + 3 * kImg;
-    uint8_t *sQ = smem + 4 * kImg;    // QS x 16 KB
-    uint8_t *sO = sQ + QS * kQBytes;  // one staging tile per group
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sO + 2 * stage_o);
-    uint64_t *kv_full = bars + 0, *kv_empty = bars + 1;
-    uint64_t *q_full = bars + 2, *q_empty = bars + 2 + kMaxQSlots;
-    uint64_t *s_full = bars + 2 + 2 * kMaxQSlots, *p_full = s_full + 2, *o_full = s_full + 4;
+    uint8_t *sQ = smem + 4 * kImg;          // kQSlots x 16 KB
+    uint8_t *sO = sQ + kQSlots * kQBytes;   // two 16 KB staging pieces
+    float *xmax = reinterpret_cast<float *>(sO + 2 * kPiece);  // [tile parity][half][row]
+    float *rsum = xmax + 2 * 2 * kTileM;                       // [buffer][half][row]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rsum + 2 * 2 * kTileM);
+    uint64_t *k_full = bars + 0, *k_empty = bars + 1, *v_full = bars + 2, *v_empty = bars + 3;
+    uint64_t *q_full = bars + 4, *q_empty = bars + 4 + kQSlots;
+    uint64_t *s_full = bars + 4 + 2 * kQSlots, *p_full = s_full + 2, *o_full = s_full + 4;
     uint64_t *tmem_free = s_full + 6;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_full + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -167,19 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long t_begin = total * blockIdx.x / gridDim.x;
     const long long t_end = total * (blockIdx.x + 1) / gridDim.x;
     const uint32_t img_bytes = (uint32_t)p.kpad * kRowBytes;
+    const KeySplit ks = key_split(p.k, p.kpad);
 
     if (tid == 0) {
-        mbar_init(kv_full, 1);
-        mbar_init(kv_empty, 1);
-        for (int s = 0; s < kMaxQSlots; ++s) {
+        mbar_init(k_full, 1);
+        mbar_init(k_empty, 1);
+        mbar_init(v_full, 1);
+        mbar_init(v_empty, 2);  // both P.V threads
+        for (int s = 0; s < kQSlots; ++s) {
             mbar_init(q_full + s, 1);
             mbar_init(q_empty + s, 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(s_full + s, 1);
-            mbar_init(p_full + s, 4);  // one arrival per warp of the group
-            mbar_init(o_full + s, 1);
-            mbar_init(tmem_free + s, 4);
+            mbar_init(p_full + s, 8);     // one arrival per softmax warp
+            mbar_init(o_full + s, 2);     // both P.V threads
+            mbar_init(tmem_free + s, 4);  // one arrival per epilogue warp
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -195,229 +336,276 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    auto terms_of = [&](int u) {
-        return p.forced_terms ? p.forced_terms : info_terms(__ldg(p.info + u));
-    };
-
     if (warp == kProducerWarp) {
-        if (lane == 0) {  // ---------------- producer: Q per tile, images per unit
-            int cur = -1, nload = 0, qit = 0;
-            for (long long T = t_begin; T < t_end; ++T) {
-                const int u = (int)(T / p.tiles_per_unit), t = (int)(T % p.tiles_per_unit);
-                const int L = valid_length(p.pad, u / p.h, p.n);
-                if (t * kTileM >= L) continue;
-                // Q first: its slot does not depend on the images of the unit.
-                const int s = qit % QS;
-                if (qit >= QS && !mbar_wait(q_empty + s, ((qit / QS) - 1) & 1, p.status, 22, abort_flag))
+        if (lane == 0) {  // ---------------- producer: Kbar images and Q tiles
+            int cur = -1, nk = 0, qit = 0;
+            for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
+                if (!wk.live()) continue;
+                const int u = wk.u, t = wk.t;
+                if (u != cur) {  // Kbar of the unit, once its predecessor's scores are done
+                    if (nk > 0 && !mbar_wait(k_empty, (nk - 1) & 1, p.status, 21, abort_flag))
+                        break;
+                    const uint8_t *src = p.images + (size_t)u * 4 * img_bytes;
+                    mbar_arrive_expect_tx(k_full, 2 * img_bytes);
+                    bulk_load(sKh, src, img_bytes, k_full);
+                    bulk_load(sKl, src + img_bytes, img_bytes, k_full);
+                    ++nk;
+                    cur = u;
+                }
+                const int s = qit % kQSlots;
+                if (qit >= kQSlots &&
+                    !mbar_wait(q_empty + s, ((qit / kQSlots) - 1) & 1, p.status, 22, abort_flag))
                     break;
                 mbar_arrive_expect_tx(q_full + s, kQBytes);
                 tma_load_3d(sQ + s * kQBytes, &tQ, q_full + s, 0, t * kTileM, u);
                 ++qit;
-                if (u != cur) {
-                    if (nload > 0 && !mbar_wait(kv_empty, (nload - 1) & 1, p.status, 21, abort_flag))
-                        break;
-                    const int terms = terms_of(u);
-                    const uint8_t *src = p.images + (size_t)u * 4 * img_bytes;
-                    mbar_arrive_expect_tx(kv_full, img_bytes * (terms == 3 ? 4u : 3u));
-                    bulk_load(sKh, src, img_bytes, kv_full);
-                    bulk_load(sKl, src + img_bytes, img_bytes, kv_full);
-                    bulk_load(sVh, src + 2 * img_bytes, img_bytes, kv_full);
-                    if (terms == 3) bulk_load(sVl, src + 3 * img_bytes, img_bytes, kv_full);
-                    cur = u;
-                    ++nload;
-                }
             }
             // Let every copy this thread started land before the CTA may exit
             // (also after an abort: a copy must not outlive the CTA).
-            if (nload > 0) mbar_wait_drain(kv_full, (nload - 1) & 1);
-            for (int i = qit > QS ? qit - QS : 0; i < qit; ++i)
-                mbar_wait_drain(q_full + (i % QS), (i / QS) & 1);
+            if (nk > 0) mbar_wait_drain(k_full, (nk - 1) & 1);
+            for (int i = qit > kQSlots ? qit - kQSlots : 0; i < qit; ++i)
+                mbar_wait_drain(q_full + (i % kQSlots), (i / kQSlots) & 1);
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {  // ---------------- MMA issuer
+    } else if (warp == kQkWarp) {
+        if (lane == 0) {  // ---------------- score products S = Q . Kbar^T, tile by tile
             const uint32_t idesc_qk = idesc_f16(128, p.kpad, 1, 0, 0);
-            const uint32_t idesc_pv = idesc_f16(128, 64, 0, 0, 1);
-            const uint32_t kh = smem_u32(sKh), kl = smem_u32(sKl);
-            const uint32_t vh = smem_u32(sVh), vl = smem_u32(sVl);
-            const int nks = p.kpad / 16;
-            // Per group: P.V products issued so far, and the product count of its
-            // latest tile (kept in registers, not local-memory arrays).
-            int cnt0 = 0, cnt1 = 0, last0 = 1, last1 = 1;
-            int cur_unit = -1, nload = 0, qit = 0;
-            long long T = t_begin;
-            auto next_tile = [&](Tile &X) -> bool {
-                while (T < t_end) {
-                    const int u = (int)(T / p.tiles_per_unit), t = (int)(T % p.tiles_per_unit);
-                    const int w = (int)((T - t_begin) & 1);
-                    ++T;
-                    if (t * kTileM < valid_length(p.pad, u / p.h, p.n)) {
-                        X = Tile{u, t, w, terms_of(u)};
-                        return true;
-                    }
+            const uint64_t dkh = sdesc(smem_u32(sKh), 16, 1024, kSwizzle128B);
+            const uint64_t dkl = sdesc(smem_u32(sKl), 16, 1024, kSwizzle128B);
+            uint32_t uses0 = 0, uses1 = 0;  // tiles that have held each buffer
+            int j = 0, cur = -1, nk = 0;
+            for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
+                if (!wk.live()) continue;
+                const int u = wk.u, w = j & 1, slot = j % kQSlots, terms = wk.terms;
+                if (u != cur) {
+                    // All score products of the previous unit are issued: its Kbar may
+                    // be replaced once they finish.
+                    if (cur >= 0) mma_commit(k_empty);
+                    if (!mbar_wait(k_full, nk & 1, p.status, 23, abort_flag)) break;
+                    ++nk;
+                    cur = u;
                 }
-                return false;
-            };
-            auto issue_qk = [&](const Tile &X) -> bool {
-                if (X.u != cur_unit) {
-                    if (nload > 0) mma_commit(kv_empty);  // old images free once issued MMAs finish
-                    if (!mbar_wait(kv_full, nload & 1, p.status, 23, abort_flag)) return false;
-                    cur_unit = X.u;
-                    ++nload;
-                }
-                const int s = qit % QS, w = X.w, o = 1 - w;
-                if (!mbar_wait(q_full + s, (qit / QS) & 1, p.status, 24, abort_flag)) return false;
-                const int cw = w ? cnt1 : cnt0, co = w ? cnt0 : cnt1, lo = w ? last0 : last1;
-                if (cw > 0 && !mbar_wait(tmem_free + w, (cw - 1) & 1, p.status, 25, abort_flag))
-                    return false;
-                if ((X.terms == 3 || lo == 3) && co > 0 &&
-                    !mbar_wait(tmem_free + o, (co - 1) & 1, p.status, 25, abort_flag))
-                    return false;
+                const uint32_t uw = w ? uses1 : uses0, uo = w ? uses0 : uses1;
+                if (uw > 0 && !mbar_wait(tmem_free + w, (uw - 1) & 1, p.status, 24, abort_flag))
+                    break;
+                if (terms == 3 && uo > 0 &&
+                    !mbar_wait(tmem_free + (w ^ 1), (uo - 1) & 1, p.status, 24, abort_flag))
+                    break;
+                if (!mbar_wait(q_full + slot, (j / kQSlots) & 1, p.status, 25, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t q0 = smem_u32(sQ + s * kQBytes);
+                const uint64_t dq = sdesc(smem_u32(sQ + slot * kQBytes), 16, 1024, kSwizzle128B);
                 const uint32_t d = tmem + kBufCols * w;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(d, sdesc(q0 + ks * 32, 16, 1024, kSwizzle128B),
-                           sdesc(kh + ks * 32, 16, 1024, kSwizzle128B), idesc_qk, ks > 0 ? 1u : 0u);
+                for (int s = 0; s < 4; ++s)
+                    mma_ss(d, dq + 2 * s, dkh + 2 * s, idesc_qk, s > 0 ? 1u : 0u);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(d, sdesc(q0 + ks * 32, 16, 1024, kSwizzle128B),
-                           sdesc(kl + ks * 32, 16, 1024, kSwizzle128B), idesc_qk, 1u);
+                for (int s = 0; s < 4; ++s) mma_ss(d, dq + 2 * s, dkl + 2 * s, idesc_qk, 1u);
                 mma_commit(s_full + w);
-                mma_commit(q_empty + s);
-                ++qit;
-                return true;
-            };
-            auto issue_pv = [&](const Tile &X) -> bool {
-                const int w = X.w, o = 1 - w;
-                if (!mbar_wait(p_full + w, (w ? cnt1 : cnt0) & 1, p.status, 26, abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t a = tmem + kBufCols * w;
-                const uint32_t dO = X.terms == 3 ? tmem + kBufCols * o + kColO : a + kColO;
-                for (int ks = 0; ks < nks; ++ks)
-                    mma_ts(dO, a + ks * 8, sdesc(vh + ks * 2048, 16, 1024, kSwizzle128B), idesc_pv,
-                           ks > 0 ? 1u : 0u);
-                if (X.terms == 3) {
-                    const uint32_t alo = tmem + kBufCols * o;
-                    for (int ks = 0; ks < nks; ++ks)
-                        mma_ts(dO, alo + ks * 8, sdesc(vh + ks * 2048, 16, 1024, kSwizzle128B),
-                               idesc_pv, 1u);
-                    for (int ks = 0; ks < nks; ++ks)
-                        mma_ts(dO, a + ks * 8, sdesc(vl + ks * 2048, 16, 1024, kSwizzle128B),
-                               idesc_pv, 1u);
+                mma_commit(q_empty + slot);
+                if (w) ++uses1;
+                else ++uses0;
+                if (terms == 3) {
+                    if (w) ++uses0;
+                    else ++uses1;
                 }
-                mma_commit(o_full + w);
-                if (w) {
-                    ++cnt1;
-                    last1 = X.terms;
-                } else {
-                    ++cnt0;
-                    last0 = X.terms;
-                }
-                return true;
-            };
-            Tile cur{}, nxt{};
-            bool have = next_tile(cur);
-            bool ok = !have || issue_qk(cur);
-            while (have && ok) {
-                const bool have_n = next_tile(nxt);
-                // Look ahead (scores of the next tile before P.V of this one) only
-                // within a unit and when both tiles use just their own buffer.
-                const bool look = have_n && nxt.u == cur.u && cur.terms == 1 && nxt.terms == 1;
-                if (look) ok = issue_qk(nxt);
-                if (ok) ok = issue_pv(cur);
-                if (ok && have_n && !look) ok = issue_qk(nxt);
-                cur = nxt;
-                have = have_n;
+                ++j;
             }
         }
         __syncwarp();
-    } else {  // ---------------- groups 0/1: softmax + epilogue, one query row per thread
-        const int w = warp >> 2;                 // group
-        const int tw = tid & 127;                // row within the tile
-        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t buf = tmem + lane_off + kBufCols * w;
-        const uint32_t other = tmem + lane_off + kBufCols * (1 - w);
-        uint8_t *stage = sO + w * stage_o;
-        const uint32_t bar_id = 1 + w;
-        int done = 0;
-        int cur_u = -1, L = 0, info = 0, terms = 1;
-        for (long long T = t_begin + w; T < t_end; T += 2) {
-            const int u = (int)(T / p.tiles_per_unit), t = (int)(T % p.tiles_per_unit);
-            if (u != cur_u) {  // per-unit values, read once per unit
-                cur_u = u;
-                L = valid_length(p.pad, u / p.h, p.n);
-                info = __ldg(p.info + u);
-                terms = p.forced_terms ? p.forced_terms : info_terms(info);
-            }
-            const int row = t * kTileM + tw;
-            // The tile row as output words: fp32 bits, or packed bf16 pairs in ov[0..31].
-            uint32_t ov[64];
-            if (t * kTileM < L) {
-                if (!warp_wait(s_full + w, done & 1, p.status, 27, abort_flag)) break;
-                tc_fence_after();
-                const float l = terms == 3 ? softmax_row<3>(buf, other, p.k, p.scale_log2)
-                                           : softmax_row<1>(buf, other, p.k, p.scale_log2);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full + w);
-                if (!warp_wait(o_full + w, done & 1, p.status, 28, abort_flag)) break;
-                tc_fence_after();
-                tmem_ld64((terms == 3 ? other : buf) + kColO, ov);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tmem_free + w);
-                ++done;
-                // Padded query rows are written as zero (selected, not scaled: their
-                // scores may hold anything, NaN included).
-                const bool valid = row < L;
-                const float inv = exp2f((float)info_exp(info)) / l;
-                if (!p.out_fp32) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        ov[i] = valid ? pack_bf16(__uint_as_float(ov[2 * i]) * inv,
-                                                  __uint_as_float(ov[2 * i + 1]) * inv)
-                                      : 0u;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        ov[i] = valid ? __float_as_uint(__uint_as_float(ov[i]) * inv) : 0u;
+    } else if (warp >= kPvWarp) {
+        if (lane == 0) {  // ---------------- O_half = P_half . Vbar_half, tile by tile
+            const int h = warp - kPvWarp;  // key half
+            const uint32_t idesc_pv = idesc_f16(128, 64, 0, 0, 1);
+            const int c0 = h ? ks.cb : 0, steps = h ? ks.s1 : ks.s0;
+            const uint32_t ocol = h ? ks.ob : ks.oa;
+            // Vbar rows of this half: the image row of key c sits at byte 128 c.
+            const uint64_t dvh =
+                sdesc(smem_u32(sVh), 16, 1024, kSwizzle128B) + (uint64_t)(c0 * kRowBytes >> 4);
+            const uint64_t dvl =
+                sdesc(smem_u32(sVl), 16, 1024, kSwizzle128B) + (uint64_t)(c0 * kRowBytes >> 4);
+            uint32_t par0 = 0, par1 = 0;
+            int j = 0, cur = -1, nv = 0;
+            bool fresh = false;  // Vbar of the current unit requested, not yet waited for
+            for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
+                if (!wk.live()) continue;
+                const int u = wk.u, w = j & 1, terms = wk.terms;
+                if (u != cur) {
+                    // The previous unit's products must finish before its Vbar is
+                    // replaced; the load is half a's job, both wait for it.
+                    if (cur >= 0) mma_commit(v_empty);
+                    if (h == 0) {
+                        if (cur >= 0 && !mbar_wait(v_empty, (nv - 1) & 1, p.status, 21, abort_flag))
+                            break;
+                        const uint8_t *src = p.images + (size_t)u * 4 * img_bytes;
+                        mbar_arrive_expect_tx(v_full, img_bytes * (terms == 3 ? 2u : 1u));
+                        bulk_load(sVh, src + 2 * img_bytes, img_bytes, v_full);
+                        if (terms == 3) bulk_load(sVl, src + 3 * img_bytes, img_bytes, v_full);
+                    }
+                    ++nv;
+                    cur = u;
+                    fresh = true;
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) ov[i] = 0u;
+                if (!mbar_wait(p_full + w, w ? par1 : par0, p.status, 26, abort_flag)) break;
+                if (w) par1 ^= 1u;
+                else par0 ^= 1u;
+                if (fresh) {
+                    if (!mbar_wait(v_full, (nv - 1) & 1, p.status, 23, abort_flag)) break;
+                    fresh = false;
+                }
+                tc_fence_after();
+                const uint32_t a = tmem + kBufCols * w + c0;          // P_half: 8 columns per step
+                const uint32_t alo = tmem + kBufCols * (w ^ 1) + c0;  // P_lo half (three products)
+                const uint32_t dO = tmem + kBufCols * w + ocol;
+                for (int s = 0; s < steps; ++s)
+                    mma_ts(dO, a + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, s > 0 ? 1u : 0u);
+                if (terms == 3) {
+                    for (int s = 0; s < steps; ++s)
+                        mma_ts(dO, alo + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, 1u);
+                    for (int s = 0; s < steps; ++s)
+                        mma_ts(dO, a + 8 * s, dvl + (uint64_t)(s * 128), idesc_pv, 1u);
+                }
+                mma_commit(o_full + w);
+                ++j;
             }
-            // Stage the tile (128-byte swizzle) once the previous store has read it.
-            if (tw == 0) bulk_wait_read0();
-            named_barrier_sync(bar_id, 128);
-            if (!p.out_fp32) {
-                uint8_t *rowp = stage + tw * kRowBytes;
+            if (h == 0 && nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1);  // no copy outlives the CTA
+        }
+        __syncwarp();
+    } else if (warp >= kEpilogueWarp) {  // ---------------- epilogue, every tile in order
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        const int tw = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const bool has_b = ks.n1 > 0;
+        int j = 0, sb = 0;
+        uint32_t par0 = 0, par1 = 0;
+        int cur_u = -1, info = 0;
+        for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
+            const int u = wk.u, t = wk.t, L = wk.L;
+            if (u != cur_u) {
+                cur_u = u;
+                info = __ldg(p.info + u);
+            }
+            const bool live_tile = wk.live();
+            float l = 1.f;
+            bool ok = true;
+            uint32_t oa[64];  // O = O_a + O_b of this row
+            if (live_tile) {
+                const int w = j & 1;
+                ++j;
+                const uint32_t par = w ? par1 : par0;
+                ok = warp_wait(p_full + w, par, p.status, 27, abort_flag);
+                if (ok) {
+                    l = rsum[(w * 2) * kTileM + tw] + rsum[(w * 2 + 1) * kTileM + tw];
+                    ok = warp_wait(o_full + w, par, p.status, 28, abort_flag);
+                }
+                if (w) par1 ^= 1u;
+                else par0 ^= 1u;
+                if (ok) {
+                    // Take all of O out of TMEM first and free the buffer at once:
+                    // the next score product into it waits for this, nothing else.
+                    tc_fence_after();
+                    const uint32_t ob_col = tmem + lane_off + kBufCols * w;
+                    tmem_ld64_async(ob_col + ks.oa, oa);
+                    if (has_b) {
+                        uint32_t ob[32];
+                        tmem_ld32_async(ob_col + ks.ob, ob);
+                        tmem_wait_ld64(oa);
+                        tmem_wait_ld(ob);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<uint4 *>(rowp + ((q ^ (tw & 7)) << 4)) =
-                        make_uint4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
-            } else {
+                        for (int i = 0; i < 32; ++i)
+                            oa[i] = __float_as_uint(__uint_as_float(oa[i]) + __uint_as_float(ob[i]));
+                        tmem_ld32_async(ob_col + ks.ob + 32, ob);
+                        tmem_wait_ld(ob);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint8_t *rowp = stage + half * 16384 + tw * kRowBytes;
+                        for (int i = 0; i < 32; ++i)
+                            oa[32 + i] =
+                                __float_as_uint(__uint_as_float(oa[32 + i]) + __uint_as_float(ob[i]));
+                    } else {
+                        tmem_wait_ld64(oa);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(tmem_free + w);
+                        if (wk.terms == 3) mbar_arrive(tmem_free + (w ^ 1));
+                    }
+                }
+            }
+            // Claim the staging buffer(s): one 16 KB piece per tile for bf16, two
+            // for fp32; the stores that last used them must have read them.  The
+            // four warps leave together if any of their waits failed.
+            if (tw == 0) {
+                if (p.out_fp32) bulk_wait_read0();
+                else bulk_wait_read1();
+            }
+            if (!named_barrier_and(kEpilogueBarrier, 128, ok)) break;
+            // Padded query rows are written as zero (selected, not scaled: their
+            // scores may hold anything, NaN included).
+            const bool valid = live_tile && t * kTileM + tw < L;
+            const uint32_t keep = valid ? 0xffffffffu : 0u;
+            // 2^e (e = the unit's Vbar scale exponent, 0..100) times 1 / row sum.
+            const float inv = __int_as_float((info_exp(info) + 127) << 23) * __frcp_rn(l);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int b0 = half * 32 + q * 4;
-                        *reinterpret_cast<uint4 *>(rowp + ((q ^ (tw & 7)) << 4)) =
-                            make_uint4(ov[b0], ov[b0 + 1], ov[b0 + 2], ov[b0 + 3]);
+            for (int i = 0; i < 64; ++i) oa[i] = keep & __float_as_uint(__uint_as_float(oa[i]) * inv);
+            if (!p.out_fp32) {  // bf16 row: 8 chunks of 16 bytes
+                uint8_t *rowp = sO + sb * kPiece + tw * kRowBytes;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w4[e] = pack_bf16(__uint_as_float(oa[8 * c + 2 * e]),
+                                          __uint_as_float(oa[8 * c + 2 * e + 1]));
+                    *reinterpret_cast<uint4 *>(rowp + ((c ^ (tw & 7)) << 4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            } else {  // fp32 row: pieces 0 (columns 0-31) and 1 (32-63)
+#pragma unroll
+                for (int pc = 0; pc < 2; ++pc) {
+                    uint8_t *rp = sO + pc * kPiece + tw * kRowBytes;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int b0 = 32 * pc + 4 * c;
+                        *reinterpret_cast<uint4 *>(rp + ((c ^ (tw & 7)) << 4)) =
+                            make_uint4(oa[b0], oa[b0 + 1], oa[b0 + 2], oa[b0 + 3]);
                     }
                 }
             }
             fence_proxy_async_smem();
-            named_barrier_sync(bar_id, 128);
+            named_barrier_sync(kEpilogueBarrier, 128);
             if (tw == 0) {
-                tma_store_3d(&tO, stage, 0, t * kTileM, u);
-                if (p.out_fp32) tma_store_3d(&tO, stage + 16384, 32, t * kTileM, u);
+                tma_store_3d(&tO, sO + sb * kPiece, 0, t * kTileM, u);
+                if (p.out_fp32) tma_store_3d(&tO, sO + kPiece, 32, t * kTileM, u);
                 bulk_commit();
             }
+            if (!p.out_fp32) sb ^= 1;
         }
         if (tw == 0) bulk_wait0();
+    } else {  // ---------------- softmax, half a row per thread
+        const int h = warp >> 2;  // key half
+        const int tw = tid & 127;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int c0 = h ? ks.cb : 0, nch = h ? ks.n1 : ks.n0;
+        int j = 0;
+        uint32_t par0 = 0, par1 = 0;
+        for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
+            if (!wk.live()) continue;
+            const int w = j & 1;
+            bool ok = warp_wait(s_full + w, w ? par1 : par0, p.status, 26, abort_flag);
+            if (w) par1 ^= 1u;
+            else par0 ^= 1u;
+            tc_fence_after();
+            float *xm = xmax + (j & 1) * 2 * kTileM;
+            const float l = softmax_half(tmem + lane_off + kBufCols * w,
+                                         tmem + lane_off + kBufCols * (w ^ 1), c0, nch, p.k,
+                                         p.scale_log2, wk.terms == 3, xm + h * kTileM + tw,
+                                         xm + (h ^ 1) * kTileM + tw, ok);
+            if (!ok) break;  // every softmax warp leaves at this tile
+            rsum[(w * 2 + h) * kTileM + tw] = l;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full + w);
+            ++j;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -427,9 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t attend_smem_bytes(int out_fp32) {
-    return 1024 + 4 * kImg + (out_fp32 ? 2 : kMaxQSlots) * kQBytes +
-           2 * (out_fp32 ? 32768 : 16384) + 256;
+size_t attend_smem_bytes(int) {
+    return 1024 + 4 * kImg + kQSlots * kQBytes + 2 * kPiece + 2 * 2 * 2 * kTileM * sizeof(float) +
+           256;
 }
 
 int launch_attend(const CUtensorMap &tQ, const CUtensorMap &tO, const AttnParams &p, int grid,

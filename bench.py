@@ -305,7 +305,8 @@ def run_ours(args):
     tfile = os.path.join(ROOT, "profiles", "traffic.json")
     if dominant and os.path.exists(tfile):
         try:
-            traffic = json.load(open(tfile)).get(dominant)
+            # dram bytes per launch from an ncu capture, keyed by workload then kernel
+            traffic = json.load(open(tfile)).get(w.name, {}).get(dominant)
         except Exception:
             traffic = None
     roofline = None

@@ -456,8 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a = tmem + kBufCols * w + c0;          // P_half: 8 columns per step
                 const uint32_t alo = tmem + kBufCols * (w ^ 1) + c0;  // P_lo half (three products)
                 const uint32_t dO = tmem + kBufCols * w + ocol;
-                for (int s = 0; s < steps; ++s)
-                    mma_ts(dO, a + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, s > 0 ? 1u : 0u);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)  // at most 8 steps of 16 keys per half
+                    if (s < steps) mma_ts(dO, a + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, s > 0 ? 1u : 0u);
                 if (terms == 3) {
                     for (int s = 0; s < steps; ++s)
                         mma_ts(dO, alo + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, 1u);

@@ -87,6 +87,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
     }
 }
 
+// One lane polls the barrier; the warp then continues together.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *status, int code,
+                                          volatile int *abort) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, status, code, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();  // orders the poller's acquire before the other lanes' reads
+    return ok != 0;
+}
+
 // Non-blocking probe of phase `parity` of `bar`.
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     uint32_t ok;

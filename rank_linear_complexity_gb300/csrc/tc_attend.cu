@@ -76,16 +76,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// One lane polls the barrier; the warp then continues together.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *status, int code,
-                                          volatile int *abort) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, status, code, abort) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();  // orders the poller's acquire before the other lanes' reads
-    return ok != 0;
-}
-
 // Split of a tile's key columns between the two softmax halves.
 struct KeySplit {
     int cb;      // first column of half b

@@ -143,62 +143,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_drain(full + (it % S), (it / S) & 1);
         }
         __syncwarp();
-    } else if (warp == 1) {  // ---------------- MMA warp (lane 0 issues, all lanes zero)
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: one thread waits, zeroes rows past the length
+        // (only in the last stage of a chunk) and issues; no warp-wide step per stage.
         const uint32_t idesc128 = idesc_f16(128, 128, 1, 0, 1);
         const uint32_t idesc64 = idesc_f16(128, 64, 1, 0, 1);
-        bool ok = true;
-        for (int it = 0; it < nkb && ok; ++it) {
-            const int s = it % S;
-            int got = 1;
-            if (lane == 0) got = mbar_wait(full + s, (it / S) & 1, p.status, 13, abort_flag) ? 1 : 0;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            __syncwarp();
-            if (!got) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint8_t *st = smem + (size_t)s * stage_bytes;
-            uint8_t *bk = st + a_bytes * (1 + p.distinct);
-            uint8_t *bv = bk + 8192;
-            const int valid = rows - it * kBK;
-            if (valid < kBK) {  // rows past the valid length count as zero
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                for (int e = lane; e < (kBK - valid) * 8; e += 32) {
-                    const int r = valid + (e >> 3), q = e & 7;
-                    reinterpret_cast<uint4 *>(bk + r * kRowBytes)[q] = z;
-                    reinterpret_cast<uint4 *>(bv + r * kRowBytes)[q] = z;
+        if (lane == 0) {
+            bool ok = true;
+            for (int it = 0; it < nkb; ++it) {
+                const int s = it % S;
+                if (!mbar_wait(full + s, (it / S) & 1, p.status, 13, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                fence_proxy_async_smem();
-            }
-            __syncwarp();
-            if (lane == 0) {
-                const uint32_t a0 = smem_u32(st), f0 = smem_u32(st + a_bytes);
-                const uint32_t k0 = smem_u32(bk), v0 = smem_u32(bv);
+                tc_fence_after();
+                uint8_t *st = smem + (size_t)s * stage_bytes;
+                uint8_t *bk = st + a_bytes * (1 + p.distinct);
+                uint8_t *bv = bk + 8192;
+                const int valid = rows - it * kBK;
+                if (valid < kBK) {  // rows past the valid length count as zero
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    for (int r = valid; r < kBK; ++r)
+                        for (int q = 0; q < 8; ++q) {
+                            reinterpret_cast<uint4 *>(bk + r * kRowBytes)[q] = z;
+                            reinterpret_cast<uint4 *>(bv + r * kRowBytes)[q] = z;
+                        }
+                    fence_proxy_async_smem();
+                }
+                // Descriptors built once per stage and stepped by adding to the address
+                // field (16-byte units): +2 per 16 K-elements of A (32 B), +1024 per
+                // 128-row half of A (16 KB), +128 per 16 rows of B (2 KB).
+                const uint64_t da = sdesc(smem_u32(st), 16, 1024, kSwizzle128B);
+                const bool two = p.mhalves == 2;
+                const uint32_t d0 = tmem, d1 = tmem + 128;
+                if (!p.distinct) {
+                    // N = 128: columns 0-63 from the K tile, 64-127 from the V tile.
+                    const uint64_t db = sdesc(smem_u32(bk), 8192, 1024, kSwizzle128B);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
-                    for (int mh = 0; mh < p.mhalves; ++mh) {
-                        const uint64_t a = sdesc(a0 + mh * 16384 + ks * 32, 16, 1024, kSwizzle128B);
-                        if (!p.distinct) {
-                            // N = 128: columns 0-63 from the K tile, 64-127 from the V tile.
-                            const uint64_t b = sdesc(k0 + ks * 2048, v0 - k0, 1024, kSwizzle128B);
-                            mma_ss(tmem + mh * 128, a, b, idesc128, acc);
-                        } else {
-                            const uint64_t b = sdesc(k0 + ks * 2048, 16, 1024, kSwizzle128B);
-                            mma_ss(tmem + mh * 128, a, b, idesc64, acc);
-                            const uint64_t af =
-                                sdesc(f0 + mh * 16384 + ks * 32, 16, 1024, kSwizzle128B);
-                            const uint64_t bvd = sdesc(v0 + ks * 2048, 16, 1024, kSwizzle128B);
-                            mma_ss(tmem + mh * 128 + 64, af, bvd, idesc64, acc);
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
+                        mma_ss(d0, da + 2 * ks, db + 128 * ks, idesc128, acc);
+                        if (two) mma_ss(d1, da + 1024 + 2 * ks, db + 128 * ks, idesc128, acc);
+                    }
+                } else {
+                    const uint64_t df = sdesc(smem_u32(st + a_bytes), 16, 1024, kSwizzle128B);
+                    const uint64_t dbk = sdesc(smem_u32(bk), 16, 1024, kSwizzle128B);
+                    const uint64_t dbv = sdesc(smem_u32(bv), 16, 1024, kSwizzle128B);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
+                        mma_ss(d0, da + 2 * ks, dbk + 128 * ks, idesc64, acc);
+                        mma_ss(d0 + 64, df + 2 * ks, dbv + 128 * ks, idesc64, acc);
+                        if (two) {
+                            mma_ss(d1, da + 1024 + 2 * ks, dbk + 128 * ks, idesc64, acc);
+                            mma_ss(d1 + 64, df + 1024 + 2 * ks, dbv + 128 * ks, idesc64, acc);
                         }
                     }
                 }
                 mma_commit(empty + s);
             }
-            __syncwarp();
-        }
-        if (lane == 0) {
             if (ok && nkb > 0)
                 mma_commit(acc_full);
             else

@@ -166,7 +166,7 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     const void *Fm = distinct ? F : E;
     CUtensorMap tE, tF, tK, tV, tQ, tO;
     const bool f32out = dtype == LINFORMER_BF16_F32OUT;
-    if (!(map3d(&tE, E, bf, 2, n, k, groups, 64, 128) && map3d(&tF, Fm, bf, 2, n, k, groups, 64, 128) &&
+    if (!(map3d(&tE, E, bf, 2, n, k, groups, 64, 128 * mhalves) && map3d(&tF, Fm, bf, 2, n, k, groups, 64, 128 * mhalves) &&
           map3d(&tK, K, bf, 2, kD, n, units, 64, kBK) && map3d(&tV, V, bf, 2, kD, n, units, 64, kBK) &&
           map3d(&tQ, Q, bf, 2, kD, n, units, 64, kTileM) &&
           (f32out ? map3d(&tO, O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, n, units, 32, kTileM)

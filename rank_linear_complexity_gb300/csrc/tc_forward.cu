@@ -103,8 +103,8 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
     const uint64_t groups = per_head ? (uint64_t)p.h : 1;
     CUtensorMap tE, tF, tK, tV;
     if (st == LINFORMER_OK &&
-        !(encode3d(&tE, p.E, bf, 2, p.n, p.k, groups, 64, 128) &&
-          encode3d(&tF, p.f_or_e(), bf, 2, p.n, p.k, groups, 64, 128) &&
+        !(encode3d(&tE, p.E, bf, 2, p.n, p.k, groups, 64, 128 * mhalves) &&
+          encode3d(&tF, p.f_or_e(), bf, 2, p.n, p.k, groups, 64, 128 * mhalves) &&
           encode3d(&tK, p.K, bf, 2, kD, p.n, units, 64, kBK) &&
           encode3d(&tV, p.V, bf, 2, kD, p.n, units, 64, kBK)))
         st = LINFORMER_ERR_LAUNCH;

@@ -3,11 +3,11 @@
 // E, F are k x n, row j of E merges the n positions into compressed position j;
 // padded rows t >= L count as zero, section Model, padding paragraph).
 //
-// One CTA owns one (unit, sequence chunk) pair.  Per 64-row stage it TMA-loads
-// the E (and F) tile, k_pad x 64, K-major, and the unit's K and V tiles,
-// 64 x 64 each, whose d axis is contiguous (MN-major operand).  One thread
-// issues tcgen05.mma into TMEM: with E = F a single N = 128 product covers K
-// and V (the E tile is read once for both); with E != F two N = 64 products.
+// One CTA owns one (unit, sequence chunk) pair.  Per 64-row stage three warps
+// TMA-load the E (and F) tile, k_pad x 64, K-major, in one box, and the unit's K
+// and V tiles, 64 x 64 each, whose d axis is contiguous (MN-major operand).  One
+// thread issues tcgen05.mma into TMEM: with E = F a single N = 128 product covers
+// K and V (the E tile is read once for both); with E != F two N = 64 products.
 // Accumulators: M-half mh (rows 128 mh ..) at TMEM columns [128 mh, 128 mh + 128),
 // columns 0-63 Kbar, 64-127 Vbar.
 //
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full + s, 1);
+            mbar_init(full + s, 3);  // the E/F, K and V loaders
             mbar_init(empty + s, 1);
         }
         mbar_init(acc_full, 1);
@@ -117,24 +117,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) {  // ---------------- TMA producer
+    if (warp != 1) {
+        // ---------------- TMA loads, one kind per warp: copies issued by one thread
+        // are handled one after another, so the E (and F) tile (one k_pad-row box)
+        // comes from warp 0, the K tile from warp 2 and the V tile from warp 3, each
+        // arming its own bytes on the stage barrier.
+        if (lane == 0) {
             int issued = 0;
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % S;
                 if (it >= S && !mbar_wait(empty + s, ((it / S) - 1) & 1, p.status, 11, abort_flag))
                     break;
                 uint8_t *st = smem + (size_t)s * stage_bytes;
-                mbar_arrive_expect_tx(full + s, stage_bytes);
-                const int x = row0 + it * kBK;
-                for (int mh = 0; mh < p.mhalves; ++mh)
-                    tma_load_3d(st + mh * 16384, &tE, full + s, x, mh * 128, gproj);
-                if (p.distinct)
-                    for (int mh = 0; mh < p.mhalves; ++mh)
-                        tma_load_3d(st + a_bytes + mh * 16384, &tF, full + s, x, mh * 128, gproj);
                 uint8_t *bk = st + a_bytes * (1 + p.distinct);
-                tma_load_3d(bk, &tK, full + s, 0, x, u);
-                tma_load_3d(bk + 8192, &tV, full + s, 0, x, u);
+                const int x = row0 + it * kBK;
+                if (warp == 0) {
+                    mbar_arrive_expect_tx(full + s, a_bytes * (1 + p.distinct));
+                    tma_load_3d(st, &tE, full + s, x, 0, gproj);
+                    if (p.distinct) tma_load_3d(st + a_bytes, &tF, full + s, x, 0, gproj);
+                } else if (warp == 2) {
+                    mbar_arrive_expect_tx(full + s, 8192);
+                    tma_load_3d(bk, &tK, full + s, 0, x, u);
+                } else {
+                    mbar_arrive_expect_tx(full + s, 8192);
+                    tma_load_3d(bk + 8192, &tV, full + s, 0, x, u);
+                }
                 issued = it + 1;
             }
             // Let every copy this thread started land before the CTA may exit

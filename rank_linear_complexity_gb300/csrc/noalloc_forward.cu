@@ -134,25 +134,12 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     uint8_t *scratch = scratch_on_current_device(&sms);
     if (!scratch) return LINFORMER_ERR_LAUNCH;
 
-    const size_t stage = (size_t)mhalves * 16384 * (1 + distinct) + 16384;
-    const int stages = (int)std::max<size_t>(2, std::min<size_t>(6, (100 * 1024) / stage));
+    const int stages = project_stages(mhalves, distinct);
     const size_t psmem = project_smem_bytes(mhalves, distinct, stages);
-    // Fewest waves of equal chunks over the resident CTA slots, among the chunk
-    // counts whose fp32 partials still fit next to the images.
-    int C = 1;
-    double best = 1e300;
-    for (int c = 1; c <= std::min(64, std::max(1, (n + 255) / 256)); ++c) {
-        const int ch = ((n + c - 1) / c + kBK - 1) / kBK * kBK;
-        const int c2 = (n + ch - 1) / ch;
-        const size_t part = round256(partial_bytes(units, c2, mhalves));
-        if (img + part + 2 * cnt > kScratchBytes) continue;
-        double cost = (double)((units * c2 + sms - 1) / sms) * (ch + 192.0) + (c2 > 1 ? 512.0 : 0.0);
-        if (pad_lengths && ch > 2048) cost *= 1.3;
-        if (cost < best - 1e-9) {
-            best = cost;
-            C = c2;
-        }
-    }
+    // The chunk count of the allocating path, among those whose fp32 partials
+    // still fit next to the images.
+    const int C = choose_chunks(n, units, sms * project_ctas_per_sm(psmem), pad_lengths != nullptr, mhalves,
+                                kScratchBytes - img - 2 * cnt);
     const int CH = ((n + C - 1) / C + kBK - 1) / kBK * kBK;
     const size_t part = round256(partial_bytes(units, C, mhalves));
     uint8_t *images = scratch;
@@ -188,6 +175,8 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     pp.C = C;
     pp.CH = CH;
     pp.stages = stages;
+    pp.prefetch = project_prefetch(CH);
+    pp.prefetch_proj = project_prefetch_proj((size_t)groups * k * n * 2 * (1 + distinct));
     pp.distinct = distinct;
     pp.per_head = per_head;
     pp.members = per_head ? b : (int)units;

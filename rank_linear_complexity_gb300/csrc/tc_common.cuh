@@ -39,26 +39,51 @@ __host__ __device__ inline size_t partial_bytes(int64_t units, int C, int mhalve
     return C > 1 ? (size_t)units * C * mhalves * 128 * 128 * sizeof(float) : 0;
 }
 
-// Fewest rows per SM: equal chunks of the sequence spread over the SMs, plus a
-// per-CTA and a split cost (in row-equivalents); unknown ragged lengths favour
-// chunks of at most 2048 rows.
-inline int choose_chunks(int n, int64_t units, int sms, bool ragged) {
-    const int max_c = n / 256 > 1 ? n / 256 : 1;
-    int best_c = 1;
-    double best = 1e300;
-    for (int c = 1; c <= (max_c < 64 ? max_c : 64); ++c) {
-        const int ch = ((n + c - 1) / c + kBK - 1) / kBK * kBK;
-        const int c2 = (n + ch - 1) / ch;
-        const double per_sm = (double)((units * c2 + sms - 1) / sms);
-        double cost = per_sm * (ch + 192.0) + (c2 > 1 ? 512.0 : 0.0);
-        if (ragged && ch > 2048) cost *= 1.3;
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_c = c2;
-        }
+// Chunks per unit for the projection.  Splitting a unit costs its CTAs a partial
+// sum written and read back, so a unit is split only as far as needed to fill one
+// wave of CTA slots (slots = SMs x CTAs resident per SM).  With ragged lengths,
+// unknown on the host, chunks are also kept to about 6144 rows or fewer so that
+// the longest valid lengths do not leave a long tail.  Chunk counts whose partial
+// sums exceed part_budget are not taken.
+inline int choose_chunks(int n, int64_t units, int slots, bool ragged, int mhalves,
+                         size_t part_budget = ~size_t(0)) {
+    const int max_c = n / 256 > 1 ? (n / 256 < 64 ? n / 256 : 64) : 1;
+    int64_t c = units > 0 ? slots / units : 1;
+    if (ragged) {
+        const int64_t r = (n + 6143) / 6144;
+        if (r > c) c = r;
     }
-    return best_c;
+    if (c < 1) c = 1;
+    if (c > max_c) c = max_c;
+    while (c > 1) {
+        const int ch = (int)(((n + c - 1) / c + kBK - 1) / kBK * kBK);
+        const int c2 = (n + ch - 1) / ch;
+        if (partial_bytes(units, c2, mhalves) <= part_budget) return c2;
+        --c;
+    }
+    return 1;
 }
+
+// Shared-memory ring depth of the projection: stages of 64 sequence rows (the E
+// and F tiles plus 8 KB each of K and V), as many as fit in about 100 KB so that
+// two CTAs share an SM, between 2 and 6.
+inline int project_stages(int mhalves, int distinct) {
+    const size_t stage = (size_t)mhalves * 16384 * (1 + distinct) + 16384;
+    const size_t s = (100 * 1024) / stage;
+    return s < 2 ? 2 : (s > 6 ? 6 : (int)s);
+}
+
+// CTAs of the projection resident per SM for a given dynamic shared-memory size.
+inline int project_ctas_per_sm(size_t smem) { return smem <= 113 * 1024 ? 2 : 1; }
+
+// L2 prefetch of the projection's tiles, issued by each loader two stages beyond
+// the shared-memory ring: K and V when a chunk runs long enough for it to pay
+// (16 stages or more); E and F only when they are too large to stay in L2 across
+// the units that share them (a prefetch of a tile already in L2 only delays the
+// loader's next copy).
+constexpr int kProjectPrefetch = 2;
+inline int project_prefetch(int chunk_rows) { return chunk_rows >= 16 * kBK ? kProjectPrefetch : 0; }
+inline int project_prefetch_proj(size_t proj_bytes) { return proj_bytes > (size_t(32) << 20) ? 1 : 0; }
 
 struct ProjParams {
     const int32_t *pad;
@@ -70,6 +95,8 @@ struct ProjParams {
     float *vbar_out;     // optional fp32 [units][k][64]
     int *status;
     int h, n, k, kpad, mhalves, C, CH, stages, distinct, per_head, members, forced_terms;
+    int prefetch;        // stages fetched into L2 ahead of the ring (0: none)
+    int prefetch_proj;   // whether the E (and F) tiles are prefetched as well
 };
 
 struct AttnParams {

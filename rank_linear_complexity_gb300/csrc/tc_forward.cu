@@ -75,11 +75,11 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
     const int mhalves = (kpad + 127) / 128;
     const int distinct = p.distinct_f() ? 1 : 0;
     const int per_head = p.proj_per_head() ? 1 : 0;
-    const size_t stage = (size_t)mhalves * 16384 * (1 + distinct) + 16384;
-    const int stages = (int)std::max<size_t>(2, std::min<size_t>(6, (100 * 1024) / stage));
+    const int stages = project_stages(mhalves, distinct);
     const size_t psmem = project_smem_bytes(mhalves, distinct, stages);
     const int sms = sm_count();
-    const int C = tc::choose_chunks(p.n, units, sms, p.pad != nullptr);
+    const int C = tc::choose_chunks(p.n, units, sms * project_ctas_per_sm(psmem), p.pad != nullptr,
+                                    mhalves);
     const int CH = ((p.n + C - 1) / C + kBK - 1) / kBK * kBK;
 
     // Workspace: images, split partials, per-unit counters and info words.
@@ -128,6 +128,8 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
         pp.C = C;
         pp.CH = CH;
         pp.stages = stages;
+        pp.prefetch = project_prefetch(CH);
+        pp.prefetch_proj = project_prefetch_proj((size_t)groups * p.k * p.n * 2 * (1 + distinct));
         pp.distinct = distinct;
         pp.per_head = per_head;
         pp.members = per_head ? p.b : (int)units;

@@ -123,6 +123,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // comes from warp 0, the K tile from warp 2 and the V tile from warp 3, each
         // arming its own bytes on the stage barrier.
         if (lane == 0) {
+            // Tiles of stage j fetched into L2 only, p.prefetch stages beyond the ring.
+            auto prefetch = [&](int j) {
+                if (j >= nkb) return;
+                const int x = row0 + j * kBK;
+                if (warp == 0) {
+                    if (!p.prefetch_proj) return;
+                    tma_prefetch_3d(&tE, x, 0, gproj);
+                    if (p.distinct) tma_prefetch_3d(&tF, x, 0, gproj);
+                } else {
+                    tma_prefetch_3d(warp == 2 ? &tK : &tV, 0, x, u);
+                }
+            };
+            for (int j = S; j < S + p.prefetch; ++j) prefetch(j);
             int issued = 0;
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % S;
@@ -143,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(bk + 8192, &tV, full + s, 0, x, u);
                 }
                 issued = it + 1;
+                if (p.prefetch > 0) prefetch(it + S + p.prefetch);
             }
             // Let every copy this thread started land before the CTA may exit
             // (also after an abort: a copy must not outlive the CTA).

@@ -186,7 +186,8 @@ LINFORMER_API const char *linformer_status_string(int status);
 LINFORMER_API int linformer_debug_read_device_status(void *stream);
 
 /* Number of products in the P.Vbar step of the tensor-core path: 0 = chosen per
- * unit on the device from max|Vbar| (default), 1 = one product (fp16 P, fp16 Vbar),
+ * unit on the device from max|Vbar| (default: 1 below 24, 2 below 40, else 3),
+ * 1 = one product (fp16 P, fp16 Vbar), 2 = P times the hi/lo split of Vbar,
  * 3 = three products (hi/lo splits of P and Vbar).  Process-wide setting for
  * tests and tuning; returns the previous value, or LINFORMER_ERR_ENUM. */
 LINFORMER_API int linformer_set_pv_terms(int terms);

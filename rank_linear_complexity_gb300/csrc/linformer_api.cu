@@ -242,7 +242,7 @@ extern "C" int linformer_debug_read_device_status(void *stream) {
 }
 
 extern "C" int linformer_set_pv_terms(int terms) {
-    if (terms != 0 && terms != 1 && terms != 3) return LINFORMER_ERR_ENUM;
+    if (terms < 0 || terms > 3) return LINFORMER_ERR_ENUM;
     return g_pv_terms.exchange(terms);
 }
 

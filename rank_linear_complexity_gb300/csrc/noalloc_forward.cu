@@ -126,7 +126,7 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     const int per_head = (share_mode == LINFORMER_SHARE_PER_HEAD ||
                           share_mode == LINFORMER_SHARE_KV) ? 1 : 0;
     const size_t img = round256((size_t)units * 4 * image_bytes(kpad));
-    const size_t cnt = round256((size_t)units * sizeof(int));
+    const size_t cnt = round256((size_t)(units + 1) * sizeof(int));  // + product-count summary
     if (img + 2 * cnt > kScratchBytes) return LINFORMER_ERR_SIZE;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -165,6 +165,7 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     pp.partial = partial;
     pp.images = images;
     pp.counters = counters;
+    pp.terms_seen = counters + units;
     pp.info = info;
     pp.status = device_status_ptr();
     pp.h = h;
@@ -188,8 +189,10 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
 
     AttnParams ap{};
     ap.pad = pad_lengths;
+    ap.out = O;
     ap.images = images;
     ap.info = info;
+    ap.terms_seen = counters + units;
     ap.status = pp.status;
     ap.h = h;
     ap.n = n;

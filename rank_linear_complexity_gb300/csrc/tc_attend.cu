@@ -59,7 +59,7 @@ constexpr uint32_t kImg = 32768;    // largest image: 256 rows x 128 bytes
 constexpr uint32_t kQBytes = 16384;
 constexpr int kQSlots = 3;
 constexpr uint32_t kPiece = 16384;  // one staged store: 128 rows x 128 bytes
-constexpr uint32_t kEpilogueBarrier = 1, kSoftmaxBarrier = 2;
+constexpr uint32_t kEpilogueBarrier = 1;
 
 __device__ __forceinline__ int valid_length(const int32_t *pad, int batch, int n) {
     if (!pad) return n;
@@ -102,35 +102,214 @@ __device__ __forceinline__ KeySplit key_split(int k, int kpad) {
     return s;
 }
 
-// Walks a CTA's contiguous range of tiles [begin, end) in unit-major order with
-// the unit, tile, valid length and product count kept up to date incrementally
-// (no per-tile 64-bit division, no per-tile global loads).
-struct TileWalk {
-    long long T, end;
-    int u, t, L, terms;
-    __device__ __forceinline__ TileWalk(const AttnParams &p, long long b, long long e)
-        : T(b), end(e), u(0), t(0), L(0), terms(1) {
-        if (T < end) {
-            u = (int)(T / p.tiles_per_unit);
-            t = (int)(T % p.tiles_per_unit);
-            load_unit(p);
+// Query tiles of a unit that hold at least one valid row, and the relative cost
+// of one such tile (by the number of P.Vbar products: measured about 1 : 1.1 : 1.9).
+__device__ __forceinline__ void unit_cost(const AttnParams &p, int u, int &live, int &weight) {
+    const int L = valid_length(p.pad, u / p.h, p.n);
+    live = (L + kTileM - 1) / kTileM;
+    const int terms = p.forced_terms ? p.forced_terms : info_terms(__ldg(p.info + u));
+    weight = terms == 1 ? 10 : (terms == 2 ? 11 : 19);
+}
+
+// A CTA's share of the work.  Live tiles (unit-major, then tile) are cut into
+// gridDim.x ranges of equal total weight: tile (u, t) starts at weight S = (the
+// weights of all live tiles before it) and belongs to CTA floor(S G / W).  Fully
+// padded tiles are cut into equal counts; their rows are written as zero.
+struct TileRanges {
+    int u0, t0, u1, t1;  // live tiles from (u0, t0) up to, not including, (u1, t1)
+    int du, dt;          // first padded tile
+    long long dn;        // number of padded tiles
+};
+
+// ceil(c X / G) for 0 <= c <= G (G > 0 at most a few thousand), from q = X / G and
+// r = X % G: c X / G = c q + c r / G with c r < G^2.
+__device__ __forceinline__ long long part_start(int c, int G, long long q, long long r) {
+    return (long long)c * q + (long long)(((unsigned)c * (unsigned)r + (unsigned)G - 1u) / (unsigned)G);
+}
+
+// The whole CTA, when lengths or costs differ between units: thread i sums units
+// [i U / T, (i+1) U / T) (T threads, at most one unit each for U <= T), a block
+// scan gives each thread's base, and the threads holding a range boundary locate
+// it within their units.  `scan` is shared scratch of 2 x (warps) 64-bit words.
+__device__ __noinline__ void split_tiles_scan(const AttnParams &p, TileRanges *r, long long *scan) {
+    constexpr int T = kThreads, NW = kThreads / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int U = p.units, G = gridDim.x, c = blockIdx.x, tpu = p.tiles_per_unit;
+    const int ua = (int)(((long long)U * tid) / T), ub = (int)(((long long)U * (tid + 1)) / T);
+    int live0 = 0, wt0 = 0;  // the thread's first unit, kept for the boundary search
+    if (ua < ub) unit_cost(p, ua, live0, wt0);
+    long long ws = (long long)live0 * wt0, ds = ua < ub ? tpu - live0 : 0;
+    for (int u = ua + 1; u < ub; ++u) {
+        int live, wt;
+        unit_cost(p, u, live, wt);
+        ws += (long long)live * wt;
+        ds += tpu - live;
+    }
+    long long wi = ws, di = ds;  // inclusive scans within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long x = __shfl_up_sync(0xffffffffu, wi, o), y = __shfl_up_sync(0xffffffffu, di, o);
+        if (lane >= o) {
+            wi += x;
+            di += y;
         }
+    }
+    if (lane == 31) {
+        scan[warp] = wi;
+        scan[NW + warp] = di;
+    }
+    if (tid == 0) {  // defaults: a boundary at the very end
+        r->u0 = r->u1 = r->du = U;
+        r->t0 = r->t1 = r->dt = 0;
+    }
+    __syncthreads();
+    long long W = 0, D = 0, wb = wi - ws, db = di - ds;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+        const long long x = scan[i], y = scan[NW + i];
+        if (i < warp) {
+            wb += x;
+            db += y;
+        }
+        W += x;
+        D += y;
+    }
+    const long long wq = W / G, wr = W - wq * G, dq = D / G, dr = D - dq * G;
+    const long long DB = part_start(c, G, dq, dr);  // the first padded tile of this CTA
+    if (tid == 0) r->dn = part_start(c + 1, G, dq, dr) - DB;
+#pragma unroll 1
+    for (int e = 0; e < 2; ++e) {  // the first live tile of this CTA and of the next
+        const long long B = part_start(c + e, G, wq, wr);
+        if (ws > 0 && wb <= B && B < wb + ws) {
+            long long acc = wb;
+            for (int u = ua; u < ub; ++u) {
+                int live = live0, wt = wt0;
+                if (u != ua) unit_cost(p, u, live, wt);
+                const long long uw = (long long)live * wt;
+                if (B < acc + uw) {
+                    const int t = (int)((B - acc + wt - 1) / wt);
+                    if (e == 0) {
+                        r->u0 = u;
+                        r->t0 = t;
+                    } else {
+                        r->u1 = u;
+                        r->t1 = t;
+                    }
+                    break;
+                }
+                acc += uw;
+            }
+        }
+    }
+    if (ds > 0 && db <= DB && DB < db + ds) {
+        long long acc = db;
+        for (int u = ua; u < ub; ++u) {
+            int live = live0, wt = wt0;
+            if (u != ua) unit_cost(p, u, live, wt);
+            if (DB < acc + (tpu - live)) {
+                r->du = u;
+                r->dt = live + (int)(DB - acc);
+                break;
+            }
+            acc += tpu - live;
+        }
+    }
+}
+
+// This CTA's ranges.  Every tile live and of one cost (no lengths, one product
+// count): equal tile counts, no scan (the same decision in every thread of every
+// CTA).  Otherwise the weighted scan, kept out of line.
+__device__ __forceinline__ void split_tiles(const AttnParams &p, TileRanges *r, long long *scan) {
+    const int U = p.units, G = gridDim.x, c = blockIdx.x, tpu = p.tiles_per_unit;
+    if (p.pad == nullptr && (p.forced_terms != 0 || __popc(__ldg(p.terms_seen)) == 1)) {
+        if (threadIdx.x == 0) {
+            const long long X = (long long)U * tpu;
+            long long b0, b1;
+            if (X * (G + 1) < (1LL << 32)) {  // 32-bit arithmetic suffices
+                b0 = ((unsigned)c * (unsigned)X + (unsigned)G - 1u) / (unsigned)G;
+                b1 = ((unsigned)(c + 1) * (unsigned)X + (unsigned)G - 1u) / (unsigned)G;
+                r->u0 = (int)((unsigned)b0 / (unsigned)tpu);
+                r->u1 = (int)((unsigned)b1 / (unsigned)tpu);
+            } else {
+                const long long q = X / G, rr = X - q * G;
+                b0 = part_start(c, G, q, rr);
+                b1 = part_start(c + 1, G, q, rr);
+                r->u0 = (int)(b0 / tpu);
+                r->u1 = (int)(b1 / tpu);
+            }
+            r->t0 = (int)(b0 - (long long)r->u0 * tpu);
+            r->t1 = (int)(b1 - (long long)r->u1 * tpu);
+            r->du = U;
+            r->dt = 0;
+            r->dn = 0;
+        }
+    } else {
+        split_tiles_scan(p, r, scan);
+    }
+}
+
+// Walks a CTA's live tiles with the unit, tile, valid length and product count
+// kept up to date incrementally (units without live tiles are passed over).
+struct TileWalk {
+    int u, t, L, live, terms, u1, t1;
+    __device__ __forceinline__ TileWalk(const AttnParams &p, const TileRanges &r)
+        : u(r.u0), t(r.t0), L(0), live(0), terms(1), u1(r.u1), t1(r.t1) {
+        if (u < p.units) load_unit(p);
+        settle(p);
     }
     __device__ __forceinline__ void load_unit(const AttnParams &p) {
         L = valid_length(p.pad, u / p.h, p.n);
+        live = (L + kTileM - 1) / kTileM;
         terms = p.forced_terms ? p.forced_terms : info_terms(__ldg(p.info + u));
     }
-    __device__ __forceinline__ bool more() const { return T < end; }
-    __device__ __forceinline__ bool live() const { return t * kTileM < L; }
-    __device__ __forceinline__ void next(const AttnParams &p) {
-        ++T;
-        if (++t == p.tiles_per_unit) {
-            t = 0;
+    __device__ __forceinline__ void settle(const AttnParams &p) {
+        while (t >= live && u < u1) {
             ++u;
-            if (T < end) load_unit(p);  // never past the last unit of the range
+            t = 0;
+            if (u < p.units) load_unit(p);
+            else live = 0;
         }
     }
+    __device__ __forceinline__ bool more() const { return u < u1 || (u == u1 && t < t1); }
+    __device__ __forceinline__ void next(const AttnParams &p) {
+        ++t;
+        settle(p);
+    }
 };
+
+// Walks a CTA's fully padded tiles: tiles [live, tiles_per_unit) of each unit.
+struct PadWalk {
+    int u, t, end;
+    long long left;
+    __device__ __forceinline__ PadWalk(const AttnParams &p, const TileRanges &r)
+        : u(r.du), t(r.dt), end(p.tiles_per_unit), left(r.dn) {
+        settle(p);
+    }
+    __device__ __forceinline__ void settle(const AttnParams &p) {
+        while (left > 0 && t >= end && u + 1 < p.units) {
+            ++u;
+            t = (valid_length(p.pad, u / p.h, p.n) + kTileM - 1) / kTileM;
+        }
+        if (t >= end) left = 0;  // nothing further (only if the count ran past the end)
+    }
+    __device__ __forceinline__ bool more() const { return left > 0; }
+    __device__ __forceinline__ void next(const AttnParams &p) {
+        ++t;
+        --left;
+        settle(p);
+    }
+};
+
+// Padded tile (u, t) written as zero with plain 16-byte stores, shared by `count`
+// threads (this one is number `idx`); the tile's rows are contiguous in O.
+__device__ __forceinline__ void zero_tile(const AttnParams &p, int u, int t, int idx, int count) {
+    const int rows = min(kTileM, p.n - t * kTileM);
+    const int chunks = rows * (p.out_fp32 ? 16 : 8);  // 16-byte chunks: 8 or 16 per row
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
+                                           ((size_t)u * p.n + (size_t)t * kTileM) *
+                                               (size_t)(p.out_fp32 ? 256 : 128));
+    for (int i = idx; i < chunks; i += count) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+}
 
 // Running row max over one 32-column chunk (MASKED: columns >= k are ignored).
 template <bool MASKED>
@@ -160,19 +339,23 @@ template <bool MASKED>
 __device__ __forceinline__ void exp_chunk(const uint32_t (&v)[32], uint32_t pcol, int c0, int k,
                                           float scale, float mb, float &l0, float &l1) {
     uint32_t ph[16];
-    const float nb = -mb;
+    const float2 sc = make_float2(scale, scale), nb = make_float2(-mb, -mb);
+    float2 acc = make_float2(l0, l1);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * e]), scale, nb));
-        float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), scale, nb));
+        const float2 x =
+            ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc, nb);
+        float p0 = ex2_approx(x.x);
+        float p1 = ex2_approx(x.y);
         if (MASKED) {
             if (c0 + 2 * e >= k) p0 = 0.f;
             if (c0 + 2 * e + 1 >= k) p1 = 0.f;
         }
         ph[e] = pack_f16(p0, p1);
-        l0 += p0;
-        l1 += p1;
+        acc = fadd2(acc, make_float2(p0, p1));
     }
+    l0 = acc.x;
+    l1 = acc.y;
     tmem_st16_async(pcol, ph);
 }
 
@@ -206,16 +389,23 @@ __device__ __forceinline__ void exp_chunk3(const uint32_t (&v)[32], uint32_t pco
     }
 }
 
+// O_a + g O_b over 32 columns: the two key halves, each normalised by its own
+// maximum, brought to the first half's (g = 2^(m_b - m_a)).
+__device__ __forceinline__ void combine_halves(uint32_t *o, const uint32_t (&ob)[32], float g) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        o[i] = __float_as_uint(fmaf(__uint_as_float(ob[i]), g, __uint_as_float(o[i])));
+}
+
 // This thread's half of one tile row: chunks [0, nch) starting at column c0 of
-// `buf` (all columns >= k are masked).  The partial max is swapped with the
-// partner thread (the other half of the row) through shared memory; returns the
-// partial row sum.  TMEM loads run one chunk ahead of the arithmetic.
+// `buf` (all columns >= k are masked), normalised by the half's own maximum, so
+// that the two halves of a row never wait for each other; the epilogue brings
+// them to the row maximum.  Returns the half's row sum and (in mb) its maximum
+// in scaled log2 units.  TMEM loads run one chunk ahead of the arithmetic.
 __device__ __forceinline__ float softmax_half(uint32_t buf, uint32_t other, int c0, int nch,
-                                              int k, float scale, bool three, float *xmine,
-                                              const float *xpartner, bool &ok) {
+                                              int k, float scale, bool three, float &mb) {
     uint32_t va[32], vb[32];
     float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-    if (!ok) nch = 0;  // this warp's wait failed: skip the work, still meet the others
     if (nch > 0) tmem_ld32_async(buf + c0, va);
 #pragma unroll 1
     for (int c = 0; c < nch; c += 2) {
@@ -231,11 +421,7 @@ __device__ __forceinline__ float softmax_half(uint32_t buf, uint32_t other, int 
             else max_chunk<true>(vb, cb, k, m0, m1, m2, m3);
         }
     }
-    const float mpart = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-    *xmine = mpart;
-    ok = named_barrier_and(kSoftmaxBarrier, 256, ok);  // all eight warps, whatever happened
-    if (!ok) return 0.f;
-    const float mb = fmaxf(mpart, *xpartner) * scale;
+    mb = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * scale;
     float l0 = 0.f, l1 = 0.f;
     if (three) {  // rare; one chunk in registers at a time
 #pragma unroll 1
@@ -280,20 +466,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sKh = smem, *sKl = smem + kImg, *sVh = smem + 2 * kImg, *sVl = smem + 3 * kImg;
     uint8_t *sQ = smem + 4 * kImg;          // kQSlots x 16 KB
     uint8_t *sO = sQ + kQSlots * kQBytes;   // two 16 KB staging pieces
-    float *xmax = reinterpret_cast<float *>(sO + 2 * kPiece);  // [tile parity][half][row]
-    float *rsum = xmax + 2 * 2 * kTileM;                       // [buffer][half][row]
+    float *rmax = reinterpret_cast<float *>(sO + 2 * kPiece);  // [buffer][half][row]
+    float *rsum = rmax + 2 * 2 * kTileM;                       // [buffer][half][row]
     uint64_t *bars = reinterpret_cast<uint64_t *>(rsum + 2 * 2 * kTileM);
     uint64_t *k_full = bars + 0, *k_empty = bars + 1, *v_full = bars + 2, *v_empty = bars + 3;
     uint64_t *q_full = bars + 4, *q_empty = bars + 4 + kQSlots;
-    uint64_t *s_full = bars + 4 + 2 * kQSlots, *p_full = s_full + 2, *o_full = s_full + 4;
-    uint64_t *tmem_free = s_full + 6;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_full + 8);
+    uint64_t *s_full = bars + 4 + 2 * kQSlots;
+    uint64_t *p_full = s_full + 2;  // [buffer][key half]
+    uint64_t *o_full = s_full + 6, *tmem_free = s_full + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_full + 10);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    TileRanges *ranges = reinterpret_cast<TileRanges *>(s_full + 11);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long total = (long long)p.units * p.tiles_per_unit;
-    const long long t_begin = total * blockIdx.x / gridDim.x;
-    const long long t_end = total * (blockIdx.x + 1) / gridDim.x;
     const uint32_t img_bytes = (uint32_t)p.kpad * kRowBytes;
     const KeySplit ks = key_split(p.k, p.kpad);
 
@@ -308,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(s_full + s, 1);
-            mbar_init(p_full + s, 8);     // one arrival per softmax warp
+            mbar_init(p_full + 2 * s, 4);      // one arrival per softmax warp of key half 0
+            mbar_init(p_full + 2 * s + 1, 4);  // ... and of key half 1
             mbar_init(o_full + s, 2);     // both P.V threads
             mbar_init(tmem_free + s, 4);  // one arrival per epilogue warp
         }
@@ -321,16 +507,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    split_tiles(p, ranges, reinterpret_cast<long long *>(rsum));  // rsum is free until the tiles
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const TileRanges rg = *ranges;
 
     if (warp == kProducerWarp) {
         if (lane == 0) {  // ---------------- producer: Kbar images and Q tiles
             int cur = -1, nk = 0, qit = 0;
-            for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
-                if (!wk.live()) continue;
+            for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
                 const int u = wk.u, t = wk.t;
                 if (u != cur) {  // Kbar of the unit, once its predecessor's scores are done
                     if (nk > 0 && !mbar_wait(k_empty, (nk - 1) & 1, p.status, 21, abort_flag))
@@ -355,6 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nk > 0) mbar_wait_drain(k_full, (nk - 1) & 1);
             for (int i = qit > kQSlots ? qit - kQSlots : 0; i < qit; ++i)
                 mbar_wait_drain(q_full + (i % kQSlots), (i / kQSlots) & 1);
+        } else {  // ---------------- the other 31 lanes: this CTA's fully padded tiles
+            for (PadWalk pw(p, rg); pw.more(); pw.next(p)) zero_tile(p, pw.u, pw.t, lane - 1, 31);
         }
         __syncwarp();
     } else if (warp == kQkWarp) {
@@ -364,8 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dkl = sdesc(smem_u32(sKl), 16, 1024, kSwizzle128B);
             uint32_t uses0 = 0, uses1 = 0;  // tiles that have held each buffer
             int j = 0, cur = -1, nk = 0;
-            for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
-                if (!wk.live()) continue;
+            for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
                 const int u = wk.u, w = j & 1, slot = j % kQSlots, terms = wk.terms;
                 if (u != cur) {
                     // All score products of the previous unit are issued: its Kbar may
@@ -416,8 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t par0 = 0, par1 = 0;
             int j = 0, cur = -1, nv = 0;
             bool fresh = false;  // Vbar of the current unit requested, not yet waited for
-            for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
-                if (!wk.live()) continue;
+            for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
                 const int u = wk.u, w = j & 1, terms = wk.terms;
                 if (u != cur) {
                     // The previous unit's products must finish before its Vbar is
@@ -427,15 +614,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (cur >= 0 && !mbar_wait(v_empty, (nv - 1) & 1, p.status, 21, abort_flag))
                             break;
                         const uint8_t *src = p.images + (size_t)u * 4 * img_bytes;
-                        mbar_arrive_expect_tx(v_full, img_bytes * (terms == 3 ? 2u : 1u));
+                        mbar_arrive_expect_tx(v_full, img_bytes * (terms >= 2 ? 2u : 1u));
                         bulk_load(sVh, src + 2 * img_bytes, img_bytes, v_full);
-                        if (terms == 3) bulk_load(sVl, src + 3 * img_bytes, img_bytes, v_full);
+                        if (terms >= 2) bulk_load(sVl, src + 3 * img_bytes, img_bytes, v_full);
                     }
                     ++nv;
                     cur = u;
                     fresh = true;
                 }
-                if (!mbar_wait(p_full + w, w ? par1 : par0, p.status, 26, abort_flag)) break;
+                if (!mbar_wait(p_full + 2 * w + h, w ? par1 : par0, p.status, 26, abort_flag)) break;
                 if (w) par1 ^= 1u;
                 else par0 ^= 1u;
                 if (fresh) {
@@ -449,11 +636,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int s = 0; s < 8; ++s)  // at most 8 steps of 16 keys per half
                     if (s < steps) mma_ts(dO, a + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, s > 0 ? 1u : 0u);
-                if (terms == 3) {
+                if (terms >= 2) {  // P_hi . Vbar_lo
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        if (s < steps) mma_ts(dO, a + 8 * s, dvl + (uint64_t)(s * 128), idesc_pv, 1u);
+                }
+                if (terms == 3) {  // P_lo . Vbar_hi
                     for (int s = 0; s < steps; ++s)
                         mma_ts(dO, alo + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, 1u);
-                    for (int s = 0; s < steps; ++s)
-                        mma_ts(dO, a + 8 * s, dvl + (uint64_t)(s * 128), idesc_pv, 1u);
                 }
                 mma_commit(o_full + w);
                 ++j;
@@ -461,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (h == 0 && nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1);  // no copy outlives the CTA
         }
         __syncwarp();
-    } else if (warp >= kEpilogueWarp) {  // ---------------- epilogue, every tile in order
+    } else if (warp >= kEpilogueWarp) {  // ---------------- epilogue, every live tile in order
         const int q = warp & 3;  // TMEM lane quarter of this warp
         const int tw = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
@@ -469,23 +659,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         int j = 0, sb = 0;
         uint32_t par0 = 0, par1 = 0;
         int cur_u = -1, info = 0;
-        for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
+        for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
             const int u = wk.u, t = wk.t, L = wk.L;
             if (u != cur_u) {
                 cur_u = u;
                 info = __ldg(p.info + u);
             }
-            const bool live_tile = wk.live();
             float l = 1.f;
             bool ok = true;
-            uint32_t oa[64];  // O = O_a + O_b of this row
-            if (live_tile) {
+            uint32_t oa[64];  // O of this row: both key halves, to the first half's maximum
+            {
                 const int w = j & 1;
                 ++j;
                 const uint32_t par = w ? par1 : par0;
-                ok = warp_wait(p_full + w, par, p.status, 27, abort_flag);
+                ok = warp_wait(p_full + 2 * w, par, p.status, 27, abort_flag) &&
+                     warp_wait(p_full + 2 * w + 1, par, p.status, 27, abort_flag);
+                // Row = (O_a + g O_b) / (l_a + g l_b), g = 2^(m_b - m_a).  g is capped
+                // at 2^100: beyond that O_a's share is below fp32 resolution anyway,
+                // and O_b g stays finite (|O_b| < 2^21).
+                float g = 0.f;
                 if (ok) {
-                    l = rsum[(w * 2) * kTileM + tw] + rsum[(w * 2 + 1) * kTileM + tw];
+                    l = rsum[(w * 2) * kTileM + tw];
+                    if (has_b) {
+                        g = ex2_approx(fminf(rmax[(w * 2 + 1) * kTileM + tw] - rmax[(w * 2) * kTileM + tw],
+                                             100.f));
+                        l = fmaf(rsum[(w * 2 + 1) * kTileM + tw], g, l);
+                    }
                     ok = warp_wait(o_full + w, par, p.status, 28, abort_flag);
                 }
                 if (w) par1 ^= 1u;
@@ -501,15 +700,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32_async(ob_col + ks.ob, ob);
                         tmem_wait_ld64(oa);
                         tmem_wait_ld(ob);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            oa[i] = __float_as_uint(__uint_as_float(oa[i]) + __uint_as_float(ob[i]));
+                        combine_halves(oa, ob, g);
                         tmem_ld32_async(ob_col + ks.ob + 32, ob);
                         tmem_wait_ld(ob);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            oa[32 + i] =
-                                __float_as_uint(__uint_as_float(oa[32 + i]) + __uint_as_float(ob[i]));
+                        combine_halves(oa + 32, ob, g);
                     } else {
                         tmem_wait_ld64(oa);
                     }
@@ -531,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!named_barrier_and(kEpilogueBarrier, 128, ok)) break;
             // Padded query rows are written as zero (selected, not scaled: their
             // scores may hold anything, NaN included).
-            const bool valid = live_tile && t * kTileM + tw < L;
+            const bool valid = t * kTileM + tw < L;
             const uint32_t keep = valid ? 0xffffffffu : 0u;
             // 2^e (e = the unit's Vbar scale exponent, 0..100) times 1 / row sum.
             const float inv = __int_as_float((info_exp(info) + 127) << 23) * __frcp_rn(l);
@@ -578,23 +772,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c0 = h ? ks.cb : 0, nch = h ? ks.n1 : ks.n0;
         int j = 0;
         uint32_t par0 = 0, par1 = 0;
-        for (TileWalk wk(p, t_begin, t_end); wk.more(); wk.next(p)) {
-            if (!wk.live()) continue;
+        for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
             const int w = j & 1;
             bool ok = warp_wait(s_full + w, w ? par1 : par0, p.status, 26, abort_flag);
             if (w) par1 ^= 1u;
             else par0 ^= 1u;
             tc_fence_after();
-            float *xm = xmax + (j & 1) * 2 * kTileM;
+            if (!ok) break;
+            float mb;
             const float l = softmax_half(tmem + lane_off + kBufCols * w,
                                          tmem + lane_off + kBufCols * (w ^ 1), c0, nch, p.k,
-                                         p.scale_log2, wk.terms == 3, xm + h * kTileM + tw,
-                                         xm + (h ^ 1) * kTileM + tw, ok);
-            if (!ok) break;  // every softmax warp leaves at this tile
+                                         p.scale_log2, wk.terms == 3, mb);
             rsum[(w * 2 + h) * kTileM + tw] = l;
+            rmax[(w * 2 + h) * kTileM + tw] = mb;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + w);
+            if (lane == 0) mbar_arrive(p_full + 2 * w + h);
             ++j;
         }
     }

@@ -21,16 +21,22 @@ constexpr int kBK = 64;          // sequence rows per projection pipeline stage
 // Vbar is stored scaled by 2^-e (e >= 0 keeps it inside the fp16 range).
 __host__ __device__ inline size_t image_bytes(int kpad) { return (size_t)kpad * kRowBytes; }
 
-// info word per unit: bits 0-7 = number of P.Vbar products (1 or 3), bits 8-15 = e.
+// info word per unit: bits 0-7 = number of P.Vbar products (1, 2 or 3), bits 8-15 = e.
 __host__ __device__ inline int pack_info(int terms, int e) { return terms | (e << 8); }
 __host__ __device__ inline int info_terms(int info) { return info & 0xff; }
 __host__ __device__ inline int info_exp(int info) { return (info >> 8) & 0xff; }
 
-// Vbar magnitude below which one fp16 product suffices for P.Vbar: the fp16
-// rounding of Vbar costs at most 2^-7 absolute below 32, and the fp16 rounding
-// of P acts as a logit perturbation of at most 2^-11, worth at most about
-// 2^-11 * max|Vbar| <= 0.0117 at 24 -- together under the 2e-2 absolute bar.
+// Vbar magnitudes that decide the number of fp16 products in P.Vbar.  O is a
+// convex combination of Vbar rows, so a relative rounding of 2^-11 in either P
+// (fp16) or Vbar (fp16) moves O by at most 2^-11 max|Vbar|.
+//   1 product, P_hi Vbar_hi: both roundings, 2^-10 max|Vbar| < 0.0235 below 24
+//     (the P part is a logit shift that mostly cancels in the normalisation).
+//   2 products, + P_hi Vbar_lo: Vbar exact to 2^-22, P's rounding only,
+//     2^-11 max|Vbar| < 0.0196 below 40.
+//   3 products, + P_lo Vbar_hi: both to about 2^-21 relative, any magnitude.
+// against an absolute bar of 2e-2 (plus 2^-8 |O| for the output rounding).
 constexpr float kOneTermMaxV = 24.0f;
+constexpr float kTwoTermMaxV = 40.0f;
 
 // Split-n partial sums: per (unit, chunk, 128-row half of k_pad) one contiguous
 // 64 KB block [128 columns][128 rows] fp32 (columns 0-63 Kbar, 64-127 Vbar), so
@@ -97,12 +103,15 @@ struct ProjParams {
     int h, n, k, kpad, mhalves, C, CH, stages, distinct, per_head, members, forced_terms;
     int prefetch;        // stages fetched into L2 ahead of the ring (0: none)
     int prefetch_proj;   // whether the E (and F) tiles are prefetched as well
+    int *terms_seen;     // bit t set if some unit takes t P.Vbar products (zero on entry)
 };
 
 struct AttnParams {
     const int32_t *pad;
+    void *out;           // O, [units][n][64] bf16 or fp32: fully padded tiles are zeroed through it
     const uint8_t *images;
     const int *info;
+    const int *terms_seen;  // bit t set if some unit takes t P.Vbar products
     int *status;
     int h, n, k, kpad, units, tiles_per_unit, forced_terms, out_fp32;
     float scale_log2;    // log2(e) / sqrt(d)

@@ -82,10 +82,11 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
                                     mhalves);
     const int CH = ((p.n + C - 1) / C + kBK - 1) / kBK * kBK;
 
-    // Workspace: images, split partials, per-unit counters and info words.
+    // Workspace: images, split partials, per-unit counters (plus the product-count
+    // summary word after them) and info words.
     const size_t img = up256(units * 4 * image_bytes(kpad));
     const size_t part = up256(partial_bytes(units, C, mhalves));
-    const size_t cnt = up256(units * sizeof(int));
+    const size_t cnt = up256((units + 1) * sizeof(int));
     char *ws = nullptr;
     if (cudaMallocAsync(reinterpret_cast<void **>(&ws), img + part + 2 * cnt, p.stream) !=
         cudaSuccess) {
@@ -116,6 +117,7 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
         pp.partial = partial;
         pp.images = images;
         pp.counters = counters;
+        pp.terms_seen = counters + units;
         pp.info = info;
         pp.kbar_out = Kbar_out;
         pp.vbar_out = Vbar_out;
@@ -150,8 +152,10 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
         } else {
             AttnParams ap{};
             ap.pad = p.pad;
+            ap.out = p.O;
             ap.images = images;
             ap.info = info;
+            ap.terms_seen = counters + units;
             ap.status = status;
             ap.h = p.h;
             ap.n = p.n;

@@ -370,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int e = 0;
         while (e < 100 && vmax * exp2f(-(float)e) >= 16384.f) ++e;
         const float vscale = exp2f(-(float)e);
-        const int terms = p.forced_terms ? p.forced_terms : (vmax < kOneTermMaxV ? 1 : 3);
+        const int terms = p.forced_terms ? p.forced_terms
+                                         : (vmax < kOneTermMaxV ? 1 : (vmax < kTwoTermMaxV ? 2 : 3));
 #pragma unroll 1
         for (int mh = 0; mh < p.mhalves; ++mh) {
             const int j = mh * 128 + jl;
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tid == 0 && ok) {
             p.info[u] = pack_info(terms, e);
+            atomicOr(p.terms_seen, 1 << terms);
             p.counters[u] = 0;
         }
     }

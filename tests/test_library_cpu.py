@@ -97,4 +97,6 @@ def test_path_selection(L):
 def test_pv_terms_setting(L):
     prev = lf.linformer_set_pv_terms(3)
     assert lf.linformer_set_pv_terms(prev) == 3
-    assert lf.linformer_set_pv_terms(2) == -4
+    assert lf.linformer_set_pv_terms(2) == prev
+    assert lf.linformer_set_pv_terms(prev) == 2
+    assert lf.linformer_set_pv_terms(4) == -4

@@ -158,6 +158,32 @@ def test_host_entry_point_matches_device():
     assert torch.equal(O_host, O_dev.cpu())
 
 
+# --- the number of P.Vbar products ------------------------------------------------------
+
+PV_CASE = (2, 3, 2048, 64, 128, PER_HEAD)  # Vbar ~ N(0, 16 vscale^2): max|Vbar| ~ 16 vscale
+
+
+@pytest.mark.parametrize("terms,vscale", [(1, 1.0), (2, 1.0), (3, 1.0), (0, 2.0), (2, 2.0),
+                                          (3, 2.0)])
+def test_pv_products_match_oracle(terms, vscale):
+    """Each forced product count where all of them meet the bar (vscale 1), and, with V
+    doubled, the per-unit choice (which then takes two products) and its neighbours."""
+    b, h, n, d, k, mode = PV_CASE
+    x = case_inputs(b, h, n, d, k, mode, BF16, seed=40)
+    x["V"] = (x["V"].float() * vscale).to(x["V"].dtype)  # a power of two: exact in bf16
+    ref, _, _, rV = orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                      mode, return_proj=True)
+    vmax = np.abs(rV).reshape(b * h, -1).max(axis=1)
+    if terms == 0:  # every unit inside the two-product band
+        assert (vmax >= 24).all() and (vmax < 40).all(), vmax
+    prev = lf.linformer_set_pv_terms(terms)
+    try:
+        O = run(x, mode, BF16)
+    finally:
+        lf.linformer_set_pv_terms(prev)
+    check(host64(O), ref, BF16, f"terms={terms} vscale={vscale}")
+
+
 # --- the five evaluation workloads at full size, sampled ------------------------------
 
 def sample_rows(n, L, rng, count=192):

@@ -453,6 +453,19 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return d;
 }
 
+// ---------------------------------------------------------------- register split
+// Per-warpgroup register budget (a multiple of 8); every warp of the warpgroup
+// executes the same instruction.  Increases wait until decreases elsewhere in the
+// CTA have returned enough registers, so the budgets must add up to the launch's.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

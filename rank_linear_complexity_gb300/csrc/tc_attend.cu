@@ -54,6 +54,11 @@ using namespace ptx;
 
 constexpr int kThreads = 512;
 constexpr int kEpilogueWarp = 8, kProducerWarp = 12, kQkWarp = 13, kPvWarp = 14;
+// Registers per thread by warpgroup (launched with 128 each): the two softmax
+// warpgroups take 136, the epilogue keeps 128, the copy and MMA-issue warpgroup
+// gives up 16.  2 x 136 + 128 + 112 = 4 x 128.
+constexpr uint32_t kSoftmaxRegs = 136, kIssueRegs = 112;
+static_assert(2 * kSoftmaxRegs + 128 + kIssueRegs == 4 * 128, "register split");
 constexpr uint32_t kBufCols = 256, kTmemCols = 512;
 constexpr uint32_t kImg = 32768;    // largest image: 256 rows x 128 bytes
 constexpr uint32_t kQBytes = 16384;
@@ -514,143 +519,146 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const TileRanges rg = *ranges;
 
-    if (warp == kProducerWarp) {
-        if (lane == 0) {  // ---------------- producer: Kbar images and Q tiles
-            int cur = -1, nk = 0, qit = 0;
-            for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
-                const int u = wk.u, t = wk.t;
-                if (u != cur) {  // Kbar of the unit, once its predecessor's scores are done
-                    if (nk > 0 && !mbar_wait(k_empty, (nk - 1) & 1, p.status, 21, abort_flag))
-                        break;
-                    const uint8_t *src = p.images + (size_t)u * 4 * img_bytes;
-                    mbar_arrive_expect_tx(k_full, 2 * img_bytes);
-                    bulk_load(sKh, src, img_bytes, k_full);
-                    bulk_load(sKl, src + img_bytes, img_bytes, k_full);
-                    ++nk;
-                    cur = u;
-                }
-                const int s = qit % kQSlots;
-                if (qit >= kQSlots &&
-                    !mbar_wait(q_empty + s, ((qit / kQSlots) - 1) & 1, p.status, 22, abort_flag))
-                    break;
-                mbar_arrive_expect_tx(q_full + s, kQBytes);
-                tma_load_3d(sQ + s * kQBytes, &tQ, q_full + s, 0, t * kTileM, u);
-                ++qit;
-            }
-            // Let every copy this thread started land before the CTA may exit
-            // (also after an abort: a copy must not outlive the CTA).
-            if (nk > 0) mbar_wait_drain(k_full, (nk - 1) & 1);
-            for (int i = qit > kQSlots ? qit - kQSlots : 0; i < qit; ++i)
-                mbar_wait_drain(q_full + (i % kQSlots), (i / kQSlots) & 1);
-        } else {  // ---------------- the other 31 lanes: this CTA's fully padded tiles
-            for (PadWalk pw(p, rg); pw.more(); pw.next(p)) zero_tile(p, pw.u, pw.t, lane - 1, 31);
-        }
-        __syncwarp();
-    } else if (warp == kQkWarp) {
-        if (lane == 0) {  // ---------------- score products S = Q . Kbar^T, tile by tile
-            const uint32_t idesc_qk = idesc_f16(128, p.kpad, 1, 0, 0);
-            const uint64_t dkh = sdesc(smem_u32(sKh), 16, 1024, kSwizzle128B);
-            const uint64_t dkl = sdesc(smem_u32(sKl), 16, 1024, kSwizzle128B);
-            uint32_t uses0 = 0, uses1 = 0;  // tiles that have held each buffer
-            int j = 0, cur = -1, nk = 0;
-            for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
-                const int u = wk.u, w = j & 1, slot = j % kQSlots, terms = wk.terms;
-                if (u != cur) {
-                    // All score products of the previous unit are issued: its Kbar may
-                    // be replaced once they finish.
-                    if (cur >= 0) mma_commit(k_empty);
-                    if (!mbar_wait(k_full, nk & 1, p.status, 23, abort_flag)) break;
-                    ++nk;
-                    cur = u;
-                }
-                const uint32_t uw = w ? uses1 : uses0, uo = w ? uses0 : uses1;
-                if (uw > 0 && !mbar_wait(tmem_free + w, (uw - 1) & 1, p.status, 24, abort_flag))
-                    break;
-                if (terms == 3 && uo > 0 &&
-                    !mbar_wait(tmem_free + (w ^ 1), (uo - 1) & 1, p.status, 24, abort_flag))
-                    break;
-                if (!mbar_wait(q_full + slot, (j / kQSlots) & 1, p.status, 25, abort_flag)) break;
-                tc_fence_after();
-                const uint64_t dq = sdesc(smem_u32(sQ + slot * kQBytes), 16, 1024, kSwizzle128B);
-                const uint32_t d = tmem + kBufCols * w;
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_ss(d, dq + 2 * s, dkh + 2 * s, idesc_qk, s > 0 ? 1u : 0u);
-#pragma unroll
-                for (int s = 0; s < 4; ++s) mma_ss(d, dq + 2 * s, dkl + 2 * s, idesc_qk, 1u);
-                mma_commit(s_full + w);
-                mma_commit(q_empty + slot);
-                if (w) ++uses1;
-                else ++uses0;
-                if (terms == 3) {
-                    if (w) ++uses0;
-                    else ++uses1;
-                }
-                ++j;
-            }
-        }
-        __syncwarp();
-    } else if (warp >= kPvWarp) {
-        if (lane == 0) {  // ---------------- O_half = P_half . Vbar_half, tile by tile
-            const int h = warp - kPvWarp;  // key half
-            const uint32_t idesc_pv = idesc_f16(128, 64, 0, 0, 1);
-            const int c0 = h ? ks.cb : 0, steps = h ? ks.s1 : ks.s0;
-            const uint32_t ocol = h ? ks.ob : ks.oa;
-            // Vbar rows of this half: the image row of key c sits at byte 128 c.
-            const uint64_t dvh =
-                sdesc(smem_u32(sVh), 16, 1024, kSwizzle128B) + (uint64_t)(c0 * kRowBytes >> 4);
-            const uint64_t dvl =
-                sdesc(smem_u32(sVl), 16, 1024, kSwizzle128B) + (uint64_t)(c0 * kRowBytes >> 4);
-            uint32_t par0 = 0, par1 = 0;
-            int j = 0, cur = -1, nv = 0;
-            bool fresh = false;  // Vbar of the current unit requested, not yet waited for
-            for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
-                const int u = wk.u, w = j & 1, terms = wk.terms;
-                if (u != cur) {
-                    // The previous unit's products must finish before its Vbar is
-                    // replaced; the load is half a's job, both wait for it.
-                    if (cur >= 0) mma_commit(v_empty);
-                    if (h == 0) {
-                        if (cur >= 0 && !mbar_wait(v_empty, (nv - 1) & 1, p.status, 21, abort_flag))
+    if (warp >= kProducerWarp) {
+        setmaxnreg_dec<kIssueRegs>();
+        if (warp == kProducerWarp) {
+            if (lane == 0) {  // ---------------- producer: Kbar images and Q tiles
+                int cur = -1, nk = 0, qit = 0;
+                for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
+                    const int u = wk.u, t = wk.t;
+                    if (u != cur) {  // Kbar of the unit, once its predecessor's scores are done
+                        if (nk > 0 && !mbar_wait(k_empty, (nk - 1) & 1, p.status, 21, abort_flag))
                             break;
                         const uint8_t *src = p.images + (size_t)u * 4 * img_bytes;
-                        mbar_arrive_expect_tx(v_full, img_bytes * (terms >= 2 ? 2u : 1u));
-                        bulk_load(sVh, src + 2 * img_bytes, img_bytes, v_full);
-                        if (terms >= 2) bulk_load(sVl, src + 3 * img_bytes, img_bytes, v_full);
+                        mbar_arrive_expect_tx(k_full, 2 * img_bytes);
+                        bulk_load(sKh, src, img_bytes, k_full);
+                        bulk_load(sKl, src + img_bytes, img_bytes, k_full);
+                        ++nk;
+                        cur = u;
                     }
-                    ++nv;
-                    cur = u;
-                    fresh = true;
+                    const int s = qit % kQSlots;
+                    if (qit >= kQSlots &&
+                        !mbar_wait(q_empty + s, ((qit / kQSlots) - 1) & 1, p.status, 22, abort_flag))
+                        break;
+                    mbar_arrive_expect_tx(q_full + s, kQBytes);
+                    tma_load_3d(sQ + s * kQBytes, &tQ, q_full + s, 0, t * kTileM, u);
+                    ++qit;
                 }
-                if (!mbar_wait(p_full + 2 * w + h, w ? par1 : par0, p.status, 26, abort_flag)) break;
-                if (w) par1 ^= 1u;
-                else par0 ^= 1u;
-                if (fresh) {
-                    if (!mbar_wait(v_full, (nv - 1) & 1, p.status, 23, abort_flag)) break;
-                    fresh = false;
-                }
-                tc_fence_after();
-                const uint32_t a = tmem + kBufCols * w + c0;          // P_half: 8 columns per step
-                const uint32_t alo = tmem + kBufCols * (w ^ 1) + c0;  // P_lo half (three products)
-                const uint32_t dO = tmem + kBufCols * w + ocol;
-#pragma unroll
-                for (int s = 0; s < 8; ++s)  // at most 8 steps of 16 keys per half
-                    if (s < steps) mma_ts(dO, a + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, s > 0 ? 1u : 0u);
-                if (terms >= 2) {  // P_hi . Vbar_lo
-#pragma unroll
-                    for (int s = 0; s < 8; ++s)
-                        if (s < steps) mma_ts(dO, a + 8 * s, dvl + (uint64_t)(s * 128), idesc_pv, 1u);
-                }
-                if (terms == 3) {  // P_lo . Vbar_hi
-                    for (int s = 0; s < steps; ++s)
-                        mma_ts(dO, alo + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, 1u);
-                }
-                mma_commit(o_full + w);
-                ++j;
+                // Let every copy this thread started land before the CTA may exit
+                // (also after an abort: a copy must not outlive the CTA).
+                if (nk > 0) mbar_wait_drain(k_full, (nk - 1) & 1);
+                for (int i = qit > kQSlots ? qit - kQSlots : 0; i < qit; ++i)
+                    mbar_wait_drain(q_full + (i % kQSlots), (i / kQSlots) & 1);
+            } else {  // ---------------- the other 31 lanes: this CTA's fully padded tiles
+                for (PadWalk pw(p, rg); pw.more(); pw.next(p)) zero_tile(p, pw.u, pw.t, lane - 1, 31);
             }
-            if (h == 0 && nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1);  // no copy outlives the CTA
+            __syncwarp();
+        } else if (warp == kQkWarp) {
+            if (lane == 0) {  // ---------------- score products S = Q . Kbar^T, tile by tile
+                const uint32_t idesc_qk = idesc_f16(128, p.kpad, 1, 0, 0);
+                const uint64_t dkh = sdesc(smem_u32(sKh), 16, 1024, kSwizzle128B);
+                const uint64_t dkl = sdesc(smem_u32(sKl), 16, 1024, kSwizzle128B);
+                uint32_t uses0 = 0, uses1 = 0;  // tiles that have held each buffer
+                int j = 0, cur = -1, nk = 0;
+                for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
+                    const int u = wk.u, w = j & 1, slot = j % kQSlots, terms = wk.terms;
+                    if (u != cur) {
+                        // All score products of the previous unit are issued: its Kbar may
+                        // be replaced once they finish.
+                        if (cur >= 0) mma_commit(k_empty);
+                        if (!mbar_wait(k_full, nk & 1, p.status, 23, abort_flag)) break;
+                        ++nk;
+                        cur = u;
+                    }
+                    const uint32_t uw = w ? uses1 : uses0, uo = w ? uses0 : uses1;
+                    if (uw > 0 && !mbar_wait(tmem_free + w, (uw - 1) & 1, p.status, 24, abort_flag))
+                        break;
+                    if (terms == 3 && uo > 0 &&
+                        !mbar_wait(tmem_free + (w ^ 1), (uo - 1) & 1, p.status, 24, abort_flag))
+                        break;
+                    if (!mbar_wait(q_full + slot, (j / kQSlots) & 1, p.status, 25, abort_flag)) break;
+                    tc_fence_after();
+                    const uint64_t dq = sdesc(smem_u32(sQ + slot * kQBytes), 16, 1024, kSwizzle128B);
+                    const uint32_t d = tmem + kBufCols * w;
+    #pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_ss(d, dq + 2 * s, dkh + 2 * s, idesc_qk, s > 0 ? 1u : 0u);
+    #pragma unroll
+                    for (int s = 0; s < 4; ++s) mma_ss(d, dq + 2 * s, dkl + 2 * s, idesc_qk, 1u);
+                    mma_commit(s_full + w);
+                    mma_commit(q_empty + slot);
+                    if (w) ++uses1;
+                    else ++uses0;
+                    if (terms == 3) {
+                        if (w) ++uses0;
+                        else ++uses1;
+                    }
+                    ++j;
+                }
+            }
+            __syncwarp();
+        } else if (warp >= kPvWarp) {
+            if (lane == 0) {  // ---------------- O_half = P_half . Vbar_half, tile by tile
+                const int h = warp - kPvWarp;  // key half
+                const uint32_t idesc_pv = idesc_f16(128, 64, 0, 0, 1);
+                const int c0 = h ? ks.cb : 0, steps = h ? ks.s1 : ks.s0;
+                const uint32_t ocol = h ? ks.ob : ks.oa;
+                // Vbar rows of this half: the image row of key c sits at byte 128 c.
+                const uint64_t dvh =
+                    sdesc(smem_u32(sVh), 16, 1024, kSwizzle128B) + (uint64_t)(c0 * kRowBytes >> 4);
+                const uint64_t dvl =
+                    sdesc(smem_u32(sVl), 16, 1024, kSwizzle128B) + (uint64_t)(c0 * kRowBytes >> 4);
+                uint32_t par0 = 0, par1 = 0;
+                int j = 0, cur = -1, nv = 0;
+                bool fresh = false;  // Vbar of the current unit requested, not yet waited for
+                for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
+                    const int u = wk.u, w = j & 1, terms = wk.terms;
+                    if (u != cur) {
+                        // The previous unit's products must finish before its Vbar is
+                        // replaced; the load is half a's job, both wait for it.
+                        if (cur >= 0) mma_commit(v_empty);
+                        if (h == 0) {
+                            if (cur >= 0 && !mbar_wait(v_empty, (nv - 1) & 1, p.status, 21, abort_flag))
+                                break;
+                            const uint8_t *src = p.images + (size_t)u * 4 * img_bytes;
+                            mbar_arrive_expect_tx(v_full, img_bytes * (terms >= 2 ? 2u : 1u));
+                            bulk_load(sVh, src + 2 * img_bytes, img_bytes, v_full);
+                            if (terms >= 2) bulk_load(sVl, src + 3 * img_bytes, img_bytes, v_full);
+                        }
+                        ++nv;
+                        cur = u;
+                        fresh = true;
+                    }
+                    if (!mbar_wait(p_full + 2 * w + h, w ? par1 : par0, p.status, 26, abort_flag)) break;
+                    if (w) par1 ^= 1u;
+                    else par0 ^= 1u;
+                    if (fresh) {
+                        if (!mbar_wait(v_full, (nv - 1) & 1, p.status, 23, abort_flag)) break;
+                        fresh = false;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = tmem + kBufCols * w + c0;          // P_half: 8 columns per step
+                    const uint32_t alo = tmem + kBufCols * (w ^ 1) + c0;  // P_lo half (three products)
+                    const uint32_t dO = tmem + kBufCols * w + ocol;
+    #pragma unroll
+                    for (int s = 0; s < 8; ++s)  // at most 8 steps of 16 keys per half
+                        if (s < steps) mma_ts(dO, a + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, s > 0 ? 1u : 0u);
+                    if (terms >= 2) {  // P_hi . Vbar_lo
+    #pragma unroll
+                        for (int s = 0; s < 8; ++s)
+                            if (s < steps) mma_ts(dO, a + 8 * s, dvl + (uint64_t)(s * 128), idesc_pv, 1u);
+                    }
+                    if (terms == 3) {  // P_lo . Vbar_hi
+                        for (int s = 0; s < steps; ++s)
+                            mma_ts(dO, alo + 8 * s, dvh + (uint64_t)(s * 128), idesc_pv, 1u);
+                    }
+                    mma_commit(o_full + w);
+                    ++j;
+                }
+                if (h == 0 && nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1);  // no copy outlives the CTA
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp >= kEpilogueWarp) {  // ---------------- epilogue, every live tile in order
         const int q = warp & 3;  // TMEM lane quarter of this warp
         const int tw = q * 32 + lane;
@@ -766,6 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tw == 0) bulk_wait0();
     } else {  // ---------------- softmax, half a row per thread
+        setmaxnreg_inc<kSoftmaxRegs>();
         const int h = warp >> 2;  // key half
         const int tw = tid & 127;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;

@@ -134,13 +134,13 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     uint8_t *scratch = scratch_on_current_device(&sms);
     if (!scratch) return LINFORMER_ERR_LAUNCH;
 
-    const int stages = project_stages(mhalves, distinct);
-    const size_t psmem = project_smem_bytes(mhalves, distinct, stages);
-    // The chunk count of the allocating path, among those whose fp32 partials
-    // still fit next to the images.
-    const int C = choose_chunks(n, units, sms * project_ctas_per_sm(psmem), pad_lengths != nullptr, mhalves,
-                                kScratchBytes - img - 2 * cnt);
-    const int CH = ((n + C - 1) / C + kBK - 1) / kBK * kBK;
+    // The allocating path's plan, among chunk counts whose fp32 partials still fit
+    // next to the images.
+    const int64_t members = per_head ? b : units;
+    const ProjPlan plan = plan_projection(n, members, units / members, mhalves, distinct,
+                                          pad_lengths != nullptr, sms, kScratchBytes - img - 2 * cnt);
+    const int C = plan.C, CH = plan.CH;
+    if (plan.smem < 1024 + kProjectMinRing + 256) return LINFORMER_ERR_UNSUPPORTED;
     const size_t part = round256(partial_bytes(units, C, mhalves));
     uint8_t *images = scratch;
     float *partial = C > 1 ? reinterpret_cast<float *>(scratch + img) : nullptr;
@@ -175,16 +175,17 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     pp.mhalves = mhalves;
     pp.C = C;
     pp.CH = CH;
-    pp.stages = stages;
+    pp.stages = plan.stages;
+    pp.stages2 = plan.stages2;
+    pp.pairs = plan.pairs;
     pp.prefetch = project_prefetch(CH);
     pp.prefetch_proj = project_prefetch_proj((size_t)groups * k * n * 2 * (1 + distinct));
     pp.distinct = distinct;
     pp.per_head = per_head;
-    pp.members = per_head ? b : (int)units;
+    pp.members = (int)members;
     pp.forced_terms = pv_terms_setting();
-    const int64_t pgrid = (int64_t)groups * C * pp.members;
-    if (pgrid > 0x7fffffffLL) return LINFORMER_ERR_SIZE;
-    int st = launch_project(tE, tF, tK, tV, pp, (int)pgrid, psmem, s);
+    if (plan.grid > 0x7fffffffLL) return LINFORMER_ERR_SIZE;
+    int st = launch_project(tE, tF, tK, tV, pp, (int)plan.grid, plan.smem, s);
     if (st != LINFORMER_OK) return st;
 
     AttnParams ap{};

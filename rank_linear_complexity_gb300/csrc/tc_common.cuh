@@ -91,6 +91,56 @@ constexpr int kProjectPrefetch = 2;
 inline int project_prefetch(int chunk_rows) { return chunk_rows >= 16 * kBK ? kProjectPrefetch : 0; }
 inline int project_prefetch_proj(size_t proj_bytes) { return proj_bytes > (size_t(32) << 20) ? 1 : 0; }
 
+// Bytes of one projection stage: the E (and F) tile plus 16 KB of K and V per unit.
+inline size_t project_stage_bytes(int mhalves, int distinct, int nunits) {
+    return (size_t)mhalves * 16384 * (1 + distinct) + (size_t)16384 * nunits;
+}
+
+// The projection's launch.  Chunks per unit as choose_chunks says; then, when units
+// are not split, E = F and lengths are absent, and one wave of CTA slots cannot give
+// every unit its own CTA, `pairs` CTAs per sharing group take two of its members:
+// one E tile per stage serves both (one N = 256 product), which takes a third less
+// traffic per unit.  With k_pad > 128 a pair fills the 512 TMEM columns, so every CTA
+// of that launch runs alone on its SM with a deeper ring.
+struct ProjPlan {
+    int C, CH;            // chunks per unit, rows per chunk
+    int stages, stages2;  // ring depth of one-unit and two-unit CTAs
+    int pairs;            // two-member CTAs per sharing group
+    size_t smem;          // dynamic shared memory per CTA
+    int64_t grid;
+};
+inline ProjPlan plan_projection(int n, int64_t members, int64_t groups, int mhalves, int distinct,
+                                bool ragged, int sms, size_t part_budget = ~size_t(0)) {
+    ProjPlan pl{};
+    const int64_t units = members * groups;
+    pl.stages = project_stages(mhalves, distinct);
+    pl.smem = 1024 + project_stage_bytes(mhalves, distinct, 1) * pl.stages + 256;
+    pl.C = choose_chunks(n, units, sms * project_ctas_per_sm(pl.smem), ragged, mhalves,
+                         part_budget);
+    pl.CH = ((n + pl.C - 1) / pl.C + kBK - 1) / kBK * kBK;
+    if (pl.C == 1 && !distinct && !ragged && members >= 2) {
+        const bool wide = mhalves == 2;
+        const size_t budget = wide ? 200 * 1024 : 100 * 1024;
+        const size_t st1 = project_stage_bytes(mhalves, 0, 1), st2 = project_stage_bytes(mhalves, 0, 2);
+        const int64_t slots = (int64_t)sms * (wide ? 1 : 2);
+        int64_t P = members - slots / groups;
+        if (P > members / 2) P = members / 2;
+        if (P > 0 && budget / st2 >= 2) {
+            pl.pairs = (int)P;
+            pl.stages = (int)(budget / st1 < 6 ? budget / st1 : 6);
+            pl.stages2 = (int)(budget / st2 < 6 ? budget / st2 : 6);
+            const size_t ring = st1 * pl.stages > st2 * pl.stages2 ? st1 * pl.stages : st2 * pl.stages2;
+            pl.smem = 1024 + ring + 256;
+        }
+    }
+    pl.grid = groups * pl.C * (members - pl.pairs);
+    return pl;
+}
+
+// The projection's split reduction reuses the ring for two 32 KB slice buffers.
+// Every plan above gives a ring of at least 96 KB.
+constexpr size_t kProjectMinRing = 64 * 1024;
+
 struct ProjParams {
     const int32_t *pad;
     float *partial;      // see partial_bytes (used when C > 1)
@@ -101,6 +151,8 @@ struct ProjParams {
     float *vbar_out;     // optional fp32 [units][k][64]
     int *status;
     int h, n, k, kpad, mhalves, C, CH, stages, distinct, per_head, members, forced_terms;
+    int pairs;           // per group and chunk: CTAs that take two members (see ProjPlan)
+    int stages2;         // ring depth of those CTAs
     int prefetch;        // stages fetched into L2 ahead of the ring (0: none)
     int prefetch_proj;   // whether the E (and F) tiles are prefetched as well
     int *terms_seen;     // bit t set if some unit takes t P.Vbar products (zero on entry)
@@ -120,7 +172,6 @@ struct AttnParams {
 int launch_project(const CUtensorMap &tE, const CUtensorMap &tF, const CUtensorMap &tK,
                    const CUtensorMap &tV, const ProjParams &p, int grid, size_t smem,
                    cudaStream_t s);
-size_t project_smem_bytes(int mhalves, int distinct, int stages);
 
 int launch_attend(const CUtensorMap &tQ, const CUtensorMap &tO, const AttnParams &p, int grid,
                   cudaStream_t s);

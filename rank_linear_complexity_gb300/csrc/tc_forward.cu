@@ -75,12 +75,12 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
     const int mhalves = (kpad + 127) / 128;
     const int distinct = p.distinct_f() ? 1 : 0;
     const int per_head = p.proj_per_head() ? 1 : 0;
-    const int stages = project_stages(mhalves, distinct);
-    const size_t psmem = project_smem_bytes(mhalves, distinct, stages);
     const int sms = sm_count();
-    const int C = tc::choose_chunks(p.n, units, sms * project_ctas_per_sm(psmem), p.pad != nullptr,
-                                    mhalves);
-    const int CH = ((p.n + C - 1) / C + kBK - 1) / kBK * kBK;
+    const int64_t members = per_head ? p.b : units;
+    const ProjPlan plan = plan_projection(p.n, members, units / members, mhalves, distinct,
+                                          p.pad != nullptr, sms);
+    const int C = plan.C, CH = plan.CH;
+    if (plan.smem < 1024 + kProjectMinRing + 256) return LINFORMER_ERR_UNSUPPORTED;
 
     // Workspace: images, split partials, per-unit counters (plus the product-count
     // summary word after them) and info words.
@@ -129,16 +129,18 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
         pp.mhalves = mhalves;
         pp.C = C;
         pp.CH = CH;
-        pp.stages = stages;
+        pp.stages = plan.stages;
+        pp.stages2 = plan.stages2;
+        pp.pairs = plan.pairs;
         pp.prefetch = project_prefetch(CH);
         pp.prefetch_proj = project_prefetch_proj((size_t)groups * p.k * p.n * 2 * (1 + distinct));
         pp.distinct = distinct;
         pp.per_head = per_head;
-        pp.members = per_head ? p.b : (int)units;
+        pp.members = (int)members;
         pp.forced_terms = pv_terms_setting();
-        const int64_t grid = groups * (int64_t)C * pp.members;
-        st = grid > 0x7fffffffLL ? LINFORMER_ERR_SIZE
-                                 : launch_project(tE, tF, tK, tV, pp, (int)grid, psmem, p.stream);
+        st = plan.grid > 0x7fffffffLL
+                 ? LINFORMER_ERR_SIZE
+                 : launch_project(tE, tF, tK, tV, pp, (int)plan.grid, plan.smem, p.stream);
     }
 
     if (st == LINFORMER_OK && !Kbar_out) {

@@ -64,13 +64,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // CTA -> (group g, chunk c, member m); members of a group share E (and F).
+    // CTA -> (group g, chunk c, slot); members of a group share E (and F).  Slots
+    // below p.pairs take members 2 slot and 2 slot + 1 (one E tile per stage for
+    // both; only unsplit units, E = F, no lengths), the others one member each.
     const int bid = blockIdx.x;
-    const int m = bid % p.members;
-    const int gc = bid / p.members;
+    const int per_group = p.members - p.pairs;
+    const int slot = bid % per_group;
+    const int gc = bid / per_group;
     const int c = gc % p.C;
     const int g = gc / p.C;
+    const int nunits = slot < p.pairs ? 2 : 1;
+    const int m = slot < p.pairs ? 2 * slot : slot + p.pairs;
     const int u = p.per_head ? m * p.h + g : m;
+    // the second unit of a pair (the next member of the same group)
+    const int u_b = p.per_head ? (m + 1) * p.h + g : m + 1;
     const int L = valid_length(p.pad, u / p.h, p.n);
     const int Cu = L > 0 ? (L + p.CH - 1) / p.CH : 1;
     if (c >= Cu) return;  // chunk entirely in the padding: nothing to add
@@ -79,9 +86,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkb = (rows + kBK - 1) / kBK;
     const int gproj = p.per_head ? g : 0;
 
+    // Stage: the E (and F) tile, then K and V tiles of 8 KB per unit, in the order
+    // K_0 V_0 K_1 V_1 (one operand of 64-column atoms 8 KB apart).
     const uint32_t a_bytes = (uint32_t)p.mhalves * 16384u;
-    const uint32_t stage_bytes = a_bytes * (1 + p.distinct) + 16384u;
-    const int S = p.stages;
+    const uint32_t stage_bytes = a_bytes * (1 + p.distinct) + 16384u * (uint32_t)nunits;
+    const int S = nunits == 2 ? p.stages2 : p.stages;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
@@ -90,7 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 2);
     float *red = reinterpret_cast<float *>(tmem_slot + 4);
-    const uint32_t ncols = (uint32_t)p.mhalves * 128u;
+    // TMEM: M-half mh at columns [128 nunits mh, ..): per unit 64 Kbar then 64 Vbar columns.
+    const uint32_t ncols = (uint32_t)(p.mhalves * nunits) * 128u;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -133,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.distinct) tma_prefetch_3d(&tF, x, 0, gproj);
                 } else {
                     tma_prefetch_3d(warp == 2 ? &tK : &tV, 0, x, u);
+                    if (nunits == 2) tma_prefetch_3d(warp == 2 ? &tK : &tV, 0, x, u_b);
                 }
             };
             for (int j = S; j < S + p.prefetch; ++j) prefetch(j);
@@ -148,12 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(full + s, a_bytes * (1 + p.distinct));
                     tma_load_3d(st, &tE, full + s, x, 0, gproj);
                     if (p.distinct) tma_load_3d(st + a_bytes, &tF, full + s, x, 0, gproj);
-                } else if (warp == 2) {
-                    mbar_arrive_expect_tx(full + s, 8192);
-                    tma_load_3d(bk, &tK, full + s, 0, x, u);
-                } else {
-                    mbar_arrive_expect_tx(full + s, 8192);
-                    tma_load_3d(bk + 8192, &tV, full + s, 0, x, u);
+                } else {  // warp 2: K tiles at +0 (+16 KB), warp 3: V tiles at +8 KB (+24 KB)
+                    const CUtensorMap *map = warp == 2 ? &tK : &tV;
+                    uint8_t *dst = bk + (warp == 2 ? 0 : 8192);
+                    mbar_arrive_expect_tx(full + s, 8192u * (uint32_t)nunits);
+                    tma_load_3d(dst, map, full + s, 0, x, u);
+                    if (nunits == 2) tma_load_3d(dst + 16384, map, full + s, 0, x, u_b);
                 }
                 issued = it + 1;
                 if (p.prefetch > 0) prefetch(it + S + p.prefetch);
@@ -168,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer: one thread waits, zeroes rows past the length
         // (only in the last stage of a chunk) and issues; no warp-wide step per stage.
         const uint32_t idesc128 = idesc_f16(128, 128, 1, 0, 1);
+        const uint32_t idesc256 = idesc_f16(128, 256, 1, 0, 1);
         const uint32_t idesc64 = idesc_f16(128, 64, 1, 0, 1);
         if (lane == 0) {
             bool ok = true;
@@ -185,10 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (valid < kBK) {  // rows past the valid length count as zero
                     const uint4 z = make_uint4(0, 0, 0, 0);
                     for (int r = valid; r < kBK; ++r)
-                        for (int q = 0; q < 8; ++q) {
-                            reinterpret_cast<uint4 *>(bk + r * kRowBytes)[q] = z;
-                            reinterpret_cast<uint4 *>(bv + r * kRowBytes)[q] = z;
-                        }
+                        for (int q = 0; q < 8 * 2 * nunits; ++q)  // K and V tiles of every unit
+                            reinterpret_cast<uint4 *>(bk + (q >> 3) * 8192 + r * kRowBytes)[q & 7] = z;
                     fence_proxy_async_smem();
                 }
                 // Descriptors built once per stage and stepped by adding to the address
@@ -196,15 +206,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // 128-row half of A (16 KB), +128 per 16 rows of B (2 KB).
                 const uint64_t da = sdesc(smem_u32(st), 16, 1024, kSwizzle128B);
                 const bool two = p.mhalves == 2;
-                const uint32_t d0 = tmem, d1 = tmem + 128;
+                const uint32_t d0 = tmem, d1 = tmem + 128 * nunits;
                 if (!p.distinct) {
-                    // N = 128: columns 0-63 from the K tile, 64-127 from the V tile.
+                    // N = 128 per unit: the unit's K tile, then its V tile (64 columns each).
                     const uint64_t db = sdesc(smem_u32(bk), 8192, 1024, kSwizzle128B);
+                    const uint32_t idesc = nunits == 2 ? idesc256 : idesc128;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
-                        mma_ss(d0, da + 2 * ks, db + 128 * ks, idesc128, acc);
-                        if (two) mma_ss(d1, da + 1024 + 2 * ks, db + 128 * ks, idesc128, acc);
+                        mma_ss(d0, da + 2 * ks, db + 128 * ks, idesc, acc);
+                        if (two) mma_ss(d1, da + 1024 + 2 * ks, db + 128 * ks, idesc, acc);
                     }
                 } else {
                     const uint64_t df = sdesc(smem_u32(st + a_bytes), 16, 1024, kSwizzle128B);
@@ -259,7 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     }
 
-    if (!aborted && (Cu == 1 || *last_flag)) {
+    // Images, info word and product count of each unit of the CTA (a pair of units
+    // only ever comes unsplit).
+#pragma unroll 1
+    for (int us = 0; us < nunits; ++us) {
+        if (aborted || !(Cu == 1 || *last_flag)) break;
+        const int uu = us ? u_b : u;
+        const uint32_t ucol = (uint32_t)us * 128u;  // the unit's columns within an M-half
         __threadfence();
         // The other chunks' sums come in as 32 KB slices (one 64-column half of one
         // 128-row block) by bulk copy into two shared buffers (the stages are idle);
@@ -271,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int mh = idx / (2 * per), rem = idx % (2 * per);
             const int half = rem / per, k2 = rem % per;
             const int c2 = k2 < c ? k2 : k2 + 1;
-            return p.partial + (((size_t)u * p.C + c2) * p.mhalves + mh) * 2 * kSlice + half * kSlice;
+            return p.partial + (((size_t)uu * p.C + c2) * p.mhalves + mh) * 2 * kSlice + half * kSlice;
         };
         int sl_issued = 0;  // slice copies started (thread 0's count)
         if (tid == 0 && nslices > 0) {
@@ -281,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(sbuf + i * kSlice, slice_src(i), kSlice * 4, fin + i);
             }
         }
-        uint8_t *img = p.images + (size_t)u * 4 * image_bytes(p.kpad);
+        uint8_t *img = p.images + (size_t)uu * 4 * image_bytes(p.kpad);
         int sidx = 0;
         float vmax = 0.f;
         bool ok = true;
@@ -290,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = mh * 128 + jl;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
-                const uint32_t tcol = lane_base + mh * 128 + half * 64;
+                const uint32_t tcol = lane_base + mh * 128 * nunits + ucol + half * 64;
                 float acc[64];
 #pragma unroll
                 for (int i = 0; i < 64; ++i) acc[i] = 0.f;
@@ -336,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 hi[e] = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
                                 lo[e] = pack_bf16(r0, r1);
                                 if (p.kbar_out && j < p.k) {
-                                    float *o = p.kbar_out + ((size_t)u * p.k + j) * kD + q * 8 + 2 * e;
+                                    float *o = p.kbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e;
                                     o[0] = __bfloat162float(h0) + __bfloat162float(__float2bfloat16_rn(r0));
                                     o[1] = __bfloat162float(h1) + __bfloat162float(__float2bfloat16_rn(r1));
                                 }
@@ -376,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int mh = 0; mh < p.mhalves; ++mh) {
             const int j = mh * 128 + jl;
             uint32_t v[64];
-            tmem_ld64(lane_base + mh * 128 + 64, v);
+            tmem_ld64(lane_base + mh * 128 * nunits + ucol + 64, v);
             if (j >= p.kpad) continue;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -390,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     hi[e2] = pack_f16(__half2float(h0), __half2float(h1));
                     lo[e2] = pack_f16(r0, r1);
                     if (p.vbar_out && j < p.k) {
-                        float *o = p.vbar_out + ((size_t)u * p.k + j) * kD + q * 8 + 2 * e2;
+                        float *o = p.vbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e2;
                         o[0] = (__half2float(h0) + __half2float(__float2half_rn(r0))) / vscale;
                         o[1] = (__half2float(h1) + __half2float(__float2half_rn(r1))) / vscale;
                     }
@@ -402,10 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (tid == 0 && ok) {
-            p.info[u] = pack_info(terms, e);
+            p.info[uu] = pack_info(terms, e);
             atomicOr(p.terms_seen, 1 << terms);
-            p.counters[u] = 0;
+            p.counters[uu] = 0;
         }
+            __syncthreads();  // red[] is reused by the next unit
     }
     tc_fence_before();
     __syncthreads();

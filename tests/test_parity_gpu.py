@@ -158,6 +158,42 @@ def test_host_entry_point_matches_device():
     assert torch.equal(O_host, O_dev.cpu())
 
 
+# --- projection CTAs that take two units ----------------------------------------------
+# More units than one wave of CTA slots, unsplit, E = F, no lengths: some CTAs project
+# two members of a sharing group with one E tile.  k > 128 gives one CTA per SM (152
+# slots), k <= 128 two (304 slots).
+
+PAIRED = [
+    # (b, h, n, k, share_mode)
+    (16, 12, 512, 256, LAYERWISE),   # 192 units: 40 two-unit CTAs
+    (16, 12, 512, 256, KV),          # per head: 4 two-member CTAs in each of 12 groups
+    (13, 12, 384, 200, KV),          # odd members: 1 pair and 11 single CTAs per group
+    (20, 16, 256, 64, LAYERWISE),    # 320 units, two CTAs per SM: 16 two-unit CTAs
+    (20, 16, 256, 64, KV),
+]
+
+
+@pytest.mark.parametrize("case", PAIRED, ids=[f"b{c[0]}h{c[1]}n{c[2]}k{c[3]}m{c[4]}"
+                                              for c in PAIRED])
+def test_paired_projection_match_oracle(case):
+    b, h, n, k, mode = case
+    x = case_inputs(b, h, n, 64, k, mode, BF16, seed=50 + b + k)
+    O = run(x, mode, BF16)
+    check(host64(O), oracle_full(x, mode), BF16, str(case))
+
+
+def test_paired_projection_outputs():
+    b, h, n, k, mode = PAIRED[0]
+    x = case_inputs(b, h, n, 64, k, mode, BF16, seed=60)
+    g = to_device(x, DEV)
+    Kb, Vb = lf.projection(g["K"], g["V"], g["E"], g["F"], g["lengths"], mode)
+    torch.cuda.synchronize()
+    _, _, rK, rV = orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"], mode,
+                                     return_proj=True)
+    for got, ref in ((host64(Kb), rK), (host64(Vb), rV)):
+        assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max() + 1e-6
+
+
 # --- the number of P.Vbar products ------------------------------------------------------
 
 PV_CASE = (2, 3, 2048, 64, 128, PER_HEAD)  # Vbar ~ N(0, 16 vscale^2): max|Vbar| ~ 16 vscale

@@ -56,6 +56,10 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// kOut: also write Kbar and Vbar in fp32 (the projection entry point).  The forward
+// pass launches the variant without that code, whose epilogue is much smaller: its
+// first execution on every SM at once is a wave of instruction fetches.
+template <bool kOut>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_project_kernel(const __grid_constant__ CUtensorMap tE, const __grid_constant__ CUtensorMap tF,
                       const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
@@ -352,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float r0 = x0 - __bfloat162float(h0), r1 = x1 - __bfloat162float(h1);
                                 hi[e] = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
                                 lo[e] = pack_bf16(r0, r1);
-                                if (p.kbar_out && j < p.k) {
+                                if (kOut && p.kbar_out && j < p.k) {
                                     float *o = p.kbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e;
                                     o[0] = __bfloat162float(h0) + __bfloat162float(__float2bfloat16_rn(r0));
                                     o[1] = __bfloat162float(h1) + __bfloat162float(__float2bfloat16_rn(r1));
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float r0 = x0 - __half2float(h0), r1 = x1 - __half2float(h1);
                     hi[e2] = pack_f16(__half2float(h0), __half2float(h1));
                     lo[e2] = pack_f16(r0, r1);
-                    if (p.vbar_out && j < p.k) {
+                    if (kOut && p.vbar_out && j < p.k) {
                         float *o = p.vbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e2;
                         o[0] = (__half2float(h0) + __half2float(__float2half_rn(r0))) / vscale;
                         o[1] = (__half2float(h1) + __half2float(__float2half_rn(r1))) / vscale;
@@ -445,13 +449,18 @@ int launch_project(const CUtensorMap &tE, const CUtensorMap &tF, const CUtensorM
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        if (cudaFuncSetAttribute(tc_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024) != cudaSuccess)
+        if (cudaFuncSetAttribute(tc_project_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
+            cudaFuncSetAttribute(tc_project_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
             return LINFORMER_ERR_LAUNCH;
         configured_dev = dev;
     }
     KernelScope scope(LINFORMER_KERNEL_PROJECT_TC, s);
-    tc_project_kernel<<<grid, kThreads, smem, s>>>(tE, tF, tK, tV, p);
+    if (p.kbar_out || p.vbar_out)
+        tc_project_kernel<true><<<grid, kThreads, smem, s>>>(tE, tF, tK, tV, p);
+    else
+        tc_project_kernel<false><<<grid, kThreads, smem, s>>>(tE, tF, tK, tV, p);
     return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
 }
 

@@ -351,15 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float x0 = acc[q * 8 + 2 * e], x1 = acc[q * 8 + 2 * e + 1];
-                                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0);
-                                const __nv_bfloat16 h1 = __float2bfloat16_rn(x1);
-                                const float r0 = x0 - __bfloat162float(h0), r1 = x1 - __bfloat162float(h1);
-                                hi[e] = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                                const float2 hf = __bfloat1622float2(h);  // exact
+                                const float r0 = x0 - hf.x, r1 = x1 - hf.y;
+                                hi[e] = *reinterpret_cast<const uint32_t *>(&h);
                                 lo[e] = pack_bf16(r0, r1);
                                 if (kOut && p.kbar_out && j < p.k) {
                                     float *o = p.kbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e;
-                                    o[0] = __bfloat162float(h0) + __bfloat162float(__float2bfloat16_rn(r0));
-                                    o[1] = __bfloat162float(h1) + __bfloat162float(__float2bfloat16_rn(r1));
+                                    o[0] = hf.x + __bfloat162float(__float2bfloat16_rn(r0));
+                                    o[1] = hf.y + __bfloat162float(__float2bfloat16_rn(r1));
                                 }
                             }
                             *image_chunk(img, j, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -367,16 +367,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         }
                     }
-                } else {  // Vbar: park the fp32 sums in TMEM until max|Vbar| is known
-                    uint32_t w0[32], w1[32];
+                } else {  // Vbar: max|Vbar| first; the images need the unit-wide scale
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        w0[i] = __float_as_uint(acc[i]);
-                        w1[i] = __float_as_uint(acc[32 + i]);
+                    for (int i = 0; i < 32; ++i)
                         vmax = fmaxf(vmax, fmaxf(fabsf(acc[i]), fabsf(acc[32 + i])));
+                    if (Cu > 1) {  // park the summed chunks in TMEM (unsplit: TMEM holds
+                                   // them already, rows past k zero since E's are)
+                        uint32_t w0[32], w1[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            w0[i] = __float_as_uint(acc[i]);
+                            w1[i] = __float_as_uint(acc[32 + i]);
+                        }
+                        tmem_st32(tcol, w0);
+                        tmem_st32(tcol + 32, w1);
                     }
-                    tmem_st32(tcol, w0);
-                    tmem_st32(tcol + 32, w1);
                 }
             }
         }
@@ -406,14 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e2 = 0; e2 < 4; ++e2) {
                     const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
                     const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
-                    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-                    const float r0 = x0 - __half2float(h0), r1 = x1 - __half2float(h1);
-                    hi[e2] = pack_f16(__half2float(h0), __half2float(h1));
+                    const __half2 h = __floats2half2_rn(x0, x1);
+                    const float2 hf = __half22float2(h);  // exact
+                    const float r0 = x0 - hf.x, r1 = x1 - hf.y;
+                    hi[e2] = *reinterpret_cast<const uint32_t *>(&h);
                     lo[e2] = pack_f16(r0, r1);
                     if (kOut && p.vbar_out && j < p.k) {
                         float *o = p.vbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e2;
-                        o[0] = (__half2float(h0) + __half2float(__float2half_rn(r0))) / vscale;
-                        o[1] = (__half2float(h1) + __half2float(__float2half_rn(r1))) / vscale;
+                        o[0] = (hf.x + __half2float(__float2half_rn(r0))) / vscale;
+                        o[1] = (hf.y + __half2float(__float2half_rn(r1))) / vscale;
                     }
                 }
                 *image_chunk(img + 2 * image_bytes(p.kpad), j, q) =

@@ -453,6 +453,18 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return d;
 }
 
+// ---------------------------------------------------------------- dependent launches
+// The next kernel in the stream, if launched with programmatic serialisation, may be
+// scheduled once every CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their writes are
+// visible (returns at once when launched without programmatic serialisation).
+__device__ __forceinline__ void wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- register split
 // Per-warpgroup register budget (a multiple of 8); every warp of the warpgroup
 // executes the same instruction.  Increases wait until decreases elsewhere in the

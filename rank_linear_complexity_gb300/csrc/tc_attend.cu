@@ -512,6 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    // Everything above overlaps the projection's last CTAs; its images and info
+    // words are read only after this.
+    wait_prerequisites();
     split_tiles(p, ranges, reinterpret_cast<long long *>(rsum));  // rsum is free until the tiles
     tc_fence_before();
     __syncthreads();
@@ -825,7 +828,22 @@ int launch_attend(const CUtensorMap &tQ, const CUtensorMap &tO, const AttnParams
         configured_dev = dev;
     }
     KernelScope scope(LINFORMER_KERNEL_ATTEND_TC, s);
-    tc_attend_kernel<<<grid, kThreads, attend_smem_bytes(p.out_fp32), s>>>(tQ, tO, p);
+    // Programmatic serialisation: the kernel may start while the projection's last
+    // CTAs finish (it waits for them before reading their output).
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = attend_smem_bytes(p.out_fp32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, tc_attend_kernel, tQ, tO, p) != cudaSuccess) {
+        cudaGetLastError();
+        return LINFORMER_ERR_LAUNCH;
+    }
     return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
 }
 

@@ -67,6 +67,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The attention kernel may take SMs as this grid's CTAs leave; it waits for the
+    // whole grid before it reads anything written here.
+    if (tid == 0) launch_dependents();
 
     // CTA -> (group g, chunk c, slot); members of a group share E (and F).  Slots
     // below p.pairs take members 2 slot and 2 slot + 1 (one E tile per stage for

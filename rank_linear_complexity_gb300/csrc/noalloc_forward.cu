@@ -185,7 +185,7 @@ extern "C" int linformer_attn_fwd_noalloc(const void *Q, const void *K, const vo
     pp.members = (int)members;
     pp.forced_terms = pv_terms_setting();
     if (plan.grid > 0x7fffffffLL) return LINFORMER_ERR_SIZE;
-    int st = launch_project(tE, tF, tK, tV, pp, (int)plan.grid, plan.smem, s);
+    int st = launch_project(tE, tF, tK, tV, pp, (int)plan.grid, plan.threads, plan.smem, s);
     if (st != LINFORMER_OK) return st;
 
     AttnParams ap{};

@@ -106,6 +106,7 @@ struct ProjPlan {
     int C, CH;            // chunks per unit, rows per chunk
     int stages, stages2;  // ring depth of one-unit and two-unit CTAs
     int pairs;            // two-member CTAs per sharing group
+    int threads;          // 128, or 256 (an eight-warp epilogue) for the one-CTA-per-SM pairs
     size_t smem;          // dynamic shared memory per CTA
     int64_t grid;
 };
@@ -133,6 +134,7 @@ inline ProjPlan plan_projection(int n, int64_t members, int64_t groups, int mhal
             pl.smem = 1024 + ring + 256;
         }
     }
+    pl.threads = pl.pairs > 0 && mhalves == 2 ? 256 : 128;
     pl.grid = groups * pl.C * (members - pl.pairs);
     return pl;
 }
@@ -169,8 +171,9 @@ struct AttnParams {
     float scale_log2;    // log2(e) / sqrt(d)
 };
 
+// threads: 128, or 256 for unsplit units without the fp32 Kbar/Vbar outputs.
 int launch_project(const CUtensorMap &tE, const CUtensorMap &tF, const CUtensorMap &tK,
-                   const CUtensorMap &tV, const ProjParams &p, int grid, size_t smem,
+                   const CUtensorMap &tV, const ProjParams &p, int grid, int threads, size_t smem,
                    cudaStream_t s);
 
 int launch_attend(const CUtensorMap &tQ, const CUtensorMap &tO, const AttnParams &p, int grid,

@@ -140,7 +140,8 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
         pp.forced_terms = pv_terms_setting();
         st = plan.grid > 0x7fffffffLL
                  ? LINFORMER_ERR_SIZE
-                 : launch_project(tE, tF, tK, tV, pp, (int)plan.grid, plan.smem, p.stream);
+                 : launch_project(tE, tF, tK, tV, pp, (int)plan.grid,
+                                  Kbar_out ? 128 : plan.threads, plan.smem, p.stream);
     }
 
     if (st == LINFORMER_OK && !Kbar_out) {

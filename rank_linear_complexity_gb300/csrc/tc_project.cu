@@ -60,7 +60,7 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
 // pass launches the variant without that code, whose epilogue is much smaller: its
 // first execution on every SM at once is a wave of instruction fetches.
 template <bool kOut>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(2 * kThreads, 1)
     tc_project_kernel(const __grid_constant__ CUtensorMap tE, const __grid_constant__ CUtensorMap tF,
                       const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
                       const ProjParams p) {
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp != 1) {
+    if (warp == 0 || warp == 2 || warp == 3) {
         // ---------------- TMA loads, one kind per warp: copies issued by one thread
         // are handled one after another, so the E (and F) tile (one k_pad-row box)
         // comes from warp 0, the K tile from warp 2 and the V tile from warp 3, each
@@ -249,14 +249,102 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
-    // ---------------- epilogue: all four warps, thread = TMEM lane = projected row
+    // ---------------- epilogue: thread = TMEM lane = projected row
     mbar_wait(acc_full, 0, p.status, 14, abort_flag);
     tc_fence_after();
     __syncthreads();
     const bool aborted = *abort_flag != 0;
-    const int jl = warp * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int jl = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
+    if (blockDim.x == 2 * kThreads) {
+        // Eight warps (launched only for unsplit units, E = F): warps 0-3 write the
+        // Kbar images while warps 4-7 find max|Vbar| and write the Vbar images.  The
+        // accumulators are final in TMEM; rows past k are zero there (so are E's).
+        const bool vgroup = warp >= 4;
+#pragma unroll 1
+        for (int us = 0; us < nunits && !aborted; ++us) {
+            const int uu = us ? u_b : u;
+            const uint32_t ucol = (uint32_t)us * 128u;
+            uint8_t *img = p.images + (size_t)uu * 4 * image_bytes(p.kpad);
+            if (!vgroup) {
+#pragma unroll 1
+                for (int mh = 0; mh < p.mhalves; ++mh) {
+                    const int j = mh * 128 + jl;
+                    uint32_t v[64];
+                    tmem_ld64(lane_base + mh * 128 * nunits + ucol, v);
+                    if (j >= p.kpad) continue;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x0 = __uint_as_float(v[q * 8 + 2 * e]);
+                            const float x1 = __uint_as_float(v[q * 8 + 2 * e + 1]);
+                            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                            const float2 hf = __bfloat1622float2(h);  // exact
+                            hi[e] = *reinterpret_cast<const uint32_t *>(&h);
+                            lo[e] = pack_bf16(x0 - hf.x, x1 - hf.y);
+                        }
+                        *image_chunk(img, j, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *image_chunk(img + image_bytes(p.kpad), j, q) =
+                            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+            } else {
+                float vmax = 0.f;
+#pragma unroll 1
+                for (int mh = 0; mh < p.mhalves; ++mh) {
+                    uint32_t v[64];
+                    tmem_ld64(lane_base + mh * 128 * nunits + ucol + 64, v);
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) vmax = fmaxf(vmax, fabsf(__uint_as_float(v[i])));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+                if (lane == 0) red[warp & 3] = vmax;
+                named_barrier_sync(1, 128);
+                vmax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+                int e = 0;
+                while (e < 100 && vmax * exp2f(-(float)e) >= 16384.f) ++e;
+                const float vscale = exp2f(-(float)e);
+                const int terms = p.forced_terms
+                                      ? p.forced_terms
+                                      : (vmax < kOneTermMaxV ? 1 : (vmax < kTwoTermMaxV ? 2 : 3));
+#pragma unroll 1
+                for (int mh = 0; mh < p.mhalves; ++mh) {
+                    const int j = mh * 128 + jl;
+                    uint32_t v[64];
+                    tmem_ld64(lane_base + mh * 128 * nunits + ucol + 64, v);
+                    if (j >= p.kpad) continue;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
+                            const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
+                            const __half2 h = __floats2half2_rn(x0, x1);
+                            const float2 hf = __half22float2(h);  // exact
+                            hi[e2] = *reinterpret_cast<const uint32_t *>(&h);
+                            lo[e2] = pack_f16(x0 - hf.x, x1 - hf.y);
+                        }
+                        *image_chunk(img + 2 * image_bytes(p.kpad), j, q) =
+                            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *image_chunk(img + 3 * image_bytes(p.kpad), j, q) =
+                            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+                if (jl == 0) {
+                    p.info[uu] = pack_info(terms, e);
+                    atomicOr(p.terms_seen, 1 << terms);
+                    p.counters[uu] = 0;
+                }
+                named_barrier_sync(1, 128);  // red[] is reused by the next unit
+            }
+        }
+    } else {
     if (!aborted && Cu > 1) {
         // This chunk's sums, [half of k_pad][column][row]: a warp stores 128 contiguous bytes.
         float *mine = p.partial + ((size_t)u * p.C + c) * p.mhalves * 2 * kSlice;
@@ -438,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
             __syncthreads();  // red[] is reused by the next unit
     }
+    }  // four-warp epilogue
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -452,8 +541,9 @@ size_t project_smem_bytes(int mhalves, int distinct, int stages) {
 }
 
 int launch_project(const CUtensorMap &tE, const CUtensorMap &tF, const CUtensorMap &tK,
-                   const CUtensorMap &tV, const ProjParams &p, int grid, size_t smem,
+                   const CUtensorMap &tV, const ProjParams &p, int grid, int threads, size_t smem,
                    cudaStream_t s) {
+    if (threads != kThreads && threads != 2 * kThreads) return LINFORMER_ERR_LAUNCH;
     static int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -467,9 +557,9 @@ int launch_project(const CUtensorMap &tE, const CUtensorMap &tF, const CUtensorM
     }
     KernelScope scope(LINFORMER_KERNEL_PROJECT_TC, s);
     if (p.kbar_out || p.vbar_out)
-        tc_project_kernel<true><<<grid, kThreads, smem, s>>>(tE, tF, tK, tV, p);
+        tc_project_kernel<true><<<grid, threads, smem, s>>>(tE, tF, tK, tV, p);
     else
-        tc_project_kernel<false><<<grid, kThreads, smem, s>>>(tE, tF, tK, tV, p);
+        tc_project_kernel<false><<<grid, threads, smem, s>>>(tE, tF, tK, tV, p);
     return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
 }
 

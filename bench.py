@@ -19,6 +19,10 @@ bounded sample of the same workload.
 
 --impl reference: the fp64 CPU oracle on the host cores, each step a bounded
 sample (whole batches) of the same workload; rank 0 only.
+
+--approx-error: not a benchmark step but the method's own approximation error
+against exact softmax attention, over n and k on the same synthetic inputs (one
+JSON line with a row per (n, k)); see approx_error_rows().
 """
 from __future__ import annotations
 
@@ -375,6 +379,75 @@ def run_ours(args):
     return 0
 
 
+# --- approximation error of the method (pages: "Linformer ... 요약 설명", sections
+# "Self-Attention is Low Rank" and "Model": the first theorem, a random projection of
+# the attention output via the Johnson-Lindenstrauss lemma, rank of order log n for a
+# fixed error; the second, a projection size that depends on the head dimension and
+# the error but not on n).  Exact references in fp64 with plain PyTorch.
+
+def full_attention64(Q, K, V):
+    """P = softmax(Q K^T / sqrt(d)) and O = P V per unit, fp64 ([..., n, d] inputs)."""
+    Q, K, V = Q.double(), K.double(), V.double()
+    P = torch.softmax(Q @ K.transpose(-1, -2) / (Q.shape[-1] ** 0.5), dim=-1)
+    return P, P @ V
+
+
+def linformer64(Q, K, V, R):
+    """The method in exact arithmetic with E = F = R (k x n): softmax(Q (R K)^T / sqrt(d)) (R V)."""
+    Q, K, V, R = Q.double(), K.double(), V.double(), R.double()
+    Kb, Vb = R @ K, R @ V
+    return torch.softmax(Q @ Kb.transpose(-1, -2) / (Q.shape[-1] ** 0.5), dim=-1) @ Vb
+
+
+def approx_errors(Q, K, V, R, O_kernel=None) -> dict:
+    """Errors for one (n, k) over units [..., n, d]:
+    - jl_t1: the first theorem's construction P R^T R V against P V, each entry divided
+      by ||p_i|| ||v_c|| (the scale of the lemma's guarantee), RMS over entries;
+    - rel_lin / jl_lin: the method's output against P V, relative in Frobenius norm and
+      normalised as jl_t1;
+    - kernel_dev: the library's output against the method in fp64 (relative Frobenius)."""
+    P, O = full_attention64(Q, K, V)
+    Rd, Vd = R.double(), V.double()
+    scale = P.norm(dim=-1, keepdim=True) * Vd.norm(dim=-2, keepdim=True)
+    T1 = (P @ Rd.transpose(-1, -2)) @ (Rd @ Vd)
+    OL = linformer64(Q, K, V, R)
+    out = {"jl_t1": float((((T1 - O) / scale) ** 2).mean().sqrt()),
+           "rel_lin": float((OL - O).norm() / O.norm()),
+           "jl_lin": float((((OL - O) / scale) ** 2).mean().sqrt())}
+    if O_kernel is not None:
+        out["kernel_dev"] = float((O_kernel.double() - OL).norm() / OL.norm())
+    return out
+
+
+def approx_error_rows(ns, ks, units=4, device="cuda:0"):
+    """One row per (n, k < n): inputs as the workloads draw them (Q, K, V ~ N(0,1),
+    one layerwise E = F ~ N(0,1/k), bf16), the library's output in fp32."""
+    import rank_linear_complexity_gb300.linformer as lf
+    from rank_linear_complexity_gb300.workloads import BF16, LAYERWISE, make_inputs
+    rows = []
+    for n in ns:
+        for k in ks:
+            if k >= n:
+                continue
+            x = make_inputs(1, units, n, 64, k, LAYERWISE, BF16, seed=4321 + n)
+            g = {kk: (v.to(device) if v is not None else None) for kk, v in x.items()}
+            O = lf.attention(g["Q"], g["K"], g["V"], g["E"], None, None, LAYERWISE, out_fp32=True)
+            torch.cuda.synchronize()
+            r = approx_errors(g["Q"][0], g["K"][0], g["V"][0], g["E"], O[0])
+            rows.append({"n": n, "k": k, **{kk: round(v, 5) for kk, v in r.items()}})
+            del g, O
+            torch.cuda.empty_cache()
+    return rows
+
+
+def run_approx_error(args):
+    rows = approx_error_rows([512, 1024, 2048, 4096], [32, 64, 128, 256])
+    print(json.dumps({"experiment": "approx_error", "units": 4, "d": 64,
+                      "inputs": "Q, K, V ~ N(0,1), one E = F ~ N(0,1/k), bf16 (workload generator)",
+                      "rows": rows}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,7 +465,11 @@ def main():
                     help="--impl reference: seconds for all warm-up + timed steps")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--approx-error", action="store_true",
+                    help="report the method's approximation error over n and k instead")
     args = ap.parse_args()
+    if args.approx_error:
+        return run_approx_error(args)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
     if args.impl == "reference":
         return run_reference(args)

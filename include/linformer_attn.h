@@ -105,7 +105,8 @@ typedef enum {
     LINFORMER_KERNEL_ATTEND_TC = 1,
     LINFORMER_KERNEL_PROJECT_SIMT = 2,
     LINFORMER_KERNEL_ATTEND_SIMT = 3,
-    LINFORMER_KERNEL_COUNT = 4
+    LINFORMER_KERNEL_WINDOW = 4,    /* linformer_window_projection */
+    LINFORMER_KERNEL_COUNT = 5
 } linformer_kernel_id;
 
 /*
@@ -172,6 +173,23 @@ LINFORMER_API int linformer_attn_fwd_noalloc(const void *Q, const void *K, const
                                              const int32_t *pad_lengths, void *O,
                                              int b, int h, int n, int d, int k,
                                              int share_mode, int dtype, void *stream);
+
+/*
+ * Pooling or convolution instead of a learned projection (요약 설명, section
+ * "Additional Efficiency Techniques").  With s = n / k (n % k == 0), writes into the
+ * caller's device buffer P, [k][n] in the input dtype (bf16 for LINFORMER_BF16 and
+ * LINFORMER_BF16_F32OUT, fp32 for LINFORMER_F32), the map whose row j averages or
+ * convolves the window of positions [j s, (j + 1) s):
+ *   weights == NULL: mean pooling, P[j][j s + t] = 1 / s (rounded to the dtype);
+ *   weights: device float[s], a convolution with kernel size = stride = s,
+ *            P[j][j s + t] = weights[t];
+ * every other entry 0.  Pass P as E (and F) of linformer_attn_fwd with a shared mode
+ * (LAYERWISE, HEADWISE), or fill one [k][n] slice per head for the per-head modes.
+ * Asynchronous on `stream`; P is owned by the caller.  Errors: LINFORMER_ERR_NULL,
+ * LINFORMER_ERR_SIZE (n % k != 0 or a size < 1), LINFORMER_ERR_ENUM, LINFORMER_ERR_LAUNCH.
+ */
+LINFORMER_API int linformer_window_projection(void *P, const float *weights, int n, int k,
+                                              int dtype, void *stream);
 
 /* Which path (linformer_path_kind) a call with these arguments takes, or a
  * negative status if the arguments are invalid.  Host only; launches nothing. */

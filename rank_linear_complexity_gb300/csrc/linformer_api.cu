@@ -276,6 +276,7 @@ extern "C" int linformer_profile_collect(double *ms, int64_t *launches) {
 
 extern "C" const char *linformer_kernel_name(int id) {
     static const char *names[LINFORMER_KERNEL_COUNT] = {
-        "tc_project_kernel", "tc_attend_kernel", "simt_project_kernel", "simt_attend_kernel"};
+        "tc_project_kernel", "tc_attend_kernel", "simt_project_kernel", "simt_attend_kernel",
+        "window_projection_kernel"};
     return (id >= 0 && id < LINFORMER_KERNEL_COUNT) ? names[id] : nullptr;
 }

@@ -17,7 +17,7 @@ from . import build as _build
 PER_HEAD, KV, HEADWISE, LAYERWISE = 0, 1, 2, 3
 F32, BF16, BF16_F32OUT = 0, 1, 2
 PATH_SIMT, PATH_TENSOR = 0, 1
-KERNEL_COUNT = 4
+KERNEL_COUNT = 5
 
 _lock = threading.Lock()
 _lib = None
@@ -30,6 +30,7 @@ SYMBOLS = [
     "linformer_select_path", "linformer_status_string", "linformer_debug_read_device_status",
     "linformer_set_pv_terms", "linformer_launch_count", "linformer_profile_enable",
     "linformer_profile_collect", "linformer_kernel_name", "linformer_attn_fwd_noalloc",
+    "linformer_window_projection",
 ]
 
 
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.linformer_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_double),
                                                     ctypes.POINTER(ctypes.c_int64)]
             L.linformer_profile_collect.restype = _i
+            L.linformer_window_projection.argtypes = [_vp, _vp, _i, _i, _i, _vp]
+            L.linformer_window_projection.restype = _i
             L.linformer_kernel_name.argtypes = [_i]
             L.linformer_kernel_name.restype = ctypes.c_char_p
             _lib = L
@@ -217,3 +220,21 @@ def projection(K, V, E, F=None, lengths=None, share_mode: int = PER_HEAD, stream
     if st != 0:
         raise LinformerError(st, "linformer_project_fwd")
     return Kb, Vb
+
+
+def linformer_window_projection(P, weights, n, k, dtype, stream=None) -> int:
+    return lib().linformer_window_projection(_ptr(P), _ptr(weights), n, k, dtype,
+                                             _stream_handle(stream))
+
+
+def window_projection(n: int, k: int, weights=None, dtype=None, device="cuda", stream=None):
+    """[k][n] device tensor: mean pooling (weights None) or a convolution with kernel =
+    stride = n / k (weights: float32 device tensor of n / k values), to pass as E (and F)."""
+    import torch
+    dt = torch.bfloat16 if dtype is None else dtype
+    P = torch.empty((k, n), dtype=dt, device=device)
+    code = F32 if dt == torch.float32 else BF16
+    st = linformer_window_projection(P, weights, n, k, code, stream)
+    if st != 0:
+        raise LinformerError(st, "linformer_window_projection")
+    return P

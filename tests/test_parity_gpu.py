@@ -170,6 +170,7 @@ PAIRED = [
     (13, 12, 384, 200, KV),          # odd members: 1 pair and 11 single CTAs per group
     (20, 16, 256, 64, LAYERWISE),    # 320 units, two CTAs per SM: 16 two-unit CTAs
     (20, 16, 256, 64, KV),
+    (16, 12, 520, 256, LAYERWISE),   # last 64-row stage partly past n in both units of a pair
 ]
 
 

@@ -4,25 +4,26 @@
 // section Transformer and Self-Attention: softmax along the key axis; padded
 // query rows produce zero output, section Model, padding paragraph).
 //
-// Persistent CTAs walk a contiguous range of 128-row query tiles (unit-major).
-// The tiles that hold query rows (the non-empty ones) alternate between two
-// 256-column TMEM buffers; tile j of the range uses buffer j % 2.
+// Persistent CTAs walk a contiguous range of live 128-row query tiles (tiles that
+// hold at least one valid row, unit-major), cut so that every CTA gets the same
+// total cost; tile j of the range uses TMEM buffer j % 2 (two 256-column buffers).
 //
 // Each tile's key columns are cut into two halves (a: columns [0, c_b),
 // b: [c_b, k)).  Roles (512 threads):
 //   warps 0-7   softmax: warp w takes TMEM lane quarter w % 4 and key half
-//               w / 4 of every tile, so one query row is shared by two
-//               threads that swap their partial maxima through shared memory;
-//               each writes its P half (fp16, packed two per column) over
-//               the scores it has read and its partial row sum to shared
-//               memory;
-//   warps 8-11  epilogue, every tile in order: O = O_a + O_b out of TMEM
-//               (which frees the buffer), scaled by 2^e / row sum, rounded,
-//               staged with the 128-byte swizzle and stored by TMA in 16 KB
-//               pieces; tiles past the valid length are written as zeros;
+//               w / 4 of every tile and normalises its half by the half's own
+//               maximum (no exchange with the other half); each writes its P
+//               half (fp16, packed two per column) over the scores it has read
+//               and its half's maximum and row sum to shared memory;
+//   warps 8-11  epilogue, every live tile in order: O = O_a + g O_b out of TMEM
+//               (g brings half b to half a's maximum; this frees the buffer),
+//               scaled by 2^e / row sum, rounded, staged with the 128-byte
+//               swizzle and stored by TMA in 16 KB pieces;
 //   warp 12     producer: Q per tile by TMA into a ring, and per unit the
 //               projection step's pre-swizzled Kbar hi/lo images by bulk copy,
 //               as soon as the previous unit's score products have finished;
+//               its other 31 lanes write the CTA's share of fully padded tiles
+//               as zeros;
 //   warp 13     one thread issues the score products of each tile once its
 //               buffer is free;
 //   warps 14-15 one thread each issues P.V of one key half once the tile's P
@@ -34,9 +35,9 @@
 //   S   = Q . Kbar_hi^T + Q . Kbar_lo^T   fp32, columns [0, k_pad)
 //   P_a over S columns [0, c_b / 2), P_b over [c_b, c_b + (k_pad - c_b) / 2)
 //   O_a = P_a . Vbar_a at column 64 (128 when k_pad <= 128), O_b at column 192
-// Units whose |Vbar| is large take three products for P . Vbar (P_lo . Vbar_hi
-// and P_hi . Vbar_lo added); P_lo then sits in the other buffer at the same
-// columns as P, so such a tile holds both buffers and runs alone.
+// Units whose |Vbar| is larger take two products for P . Vbar (P_hi . Vbar_lo
+// added) or, larger still, three (P_lo . Vbar_hi too); P_lo then sits in the other
+// buffer at the same columns as P, so such a tile holds both buffers and runs alone.
 // The softmax is exact and two-pass (row max, then exp2 with the 1/sqrt(d)
 // scale folded in, row sum); scores never leave the SM.
 #include <cuda_bf16.h>

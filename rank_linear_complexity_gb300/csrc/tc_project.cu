@@ -3,13 +3,16 @@
 // E, F are k x n, row j of E merges the n positions into compressed position j;
 // padded rows t >= L count as zero, section Model, padding paragraph).
 //
-// One CTA owns one (unit, sequence chunk) pair.  Per 64-row stage three warps
-// TMA-load the E (and F) tile, k_pad x 64, K-major, in one box, and the unit's K
-// and V tiles, 64 x 64 each, whose d axis is contiguous (MN-major operand).  One
-// thread issues tcgen05.mma into TMEM: with E = F a single N = 128 product covers
-// K and V (the E tile is read once for both); with E != F two N = 64 products.
-// Accumulators: M-half mh (rows 128 mh ..) at TMEM columns [128 mh, 128 mh + 128),
-// columns 0-63 Kbar, 64-127 Vbar.
+// One CTA owns one (unit, sequence chunk) pair, or two unsplit units of the same
+// sharing group (E = F, no lengths).  Per 64-row stage three warps TMA-load the E
+// (and F) tile, k_pad x 64, K-major, in one box, and each unit's K and V tiles,
+// 64 x 64 each, whose d axis is contiguous (MN-major operand).  One thread issues
+// tcgen05.mma into TMEM: with E = F a single product of N = 128 per unit covers K
+// and V (the E tile is read once for all of them); with E != F two N = 64 products.
+// Accumulators: M-half mh (rows 128 mh ..) at TMEM columns [128 u mh, ..) for u
+// units, per unit 64 Kbar columns then 64 Vbar columns.  The epilogue turns them into
+// the images the attention step reads, with four warps, or with eight (Kbar and Vbar
+// in parallel) when the launch runs one CTA per SM.
 //
 // Chunks of the same unit are summed in a fixed order (chunk 0, 1, ...) by
 // whichever CTA of the unit arrives last, so the result does not depend on

@@ -39,8 +39,10 @@
  * Ownership: the caller owns every buffer.  All pointers of linformer_attn_fwd
  * and linformer_project_fwd are device pointers of the current CUDA device, 16-byte
  * aligned.  The library writes only O (or Kbar/Vbar) and a stream-ordered
- * workspace that it allocates and frees on `stream` (cudaMallocAsync /
- * cudaFreeAsync).  Calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ * workspace that it allocates and frees on `stream` (cudaMallocFromPoolAsync /
+ * cudaFreeAsync) from a memory pool of its own per device, created on first use,
+ * which keeps freed memory mapped for the next call until the process exits (as much
+ * as the largest call in flight needed).  Calls are asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream): inputs must stay unchanged until the stream has
  * passed the call.  Calls on different streams may run concurrently.
  *

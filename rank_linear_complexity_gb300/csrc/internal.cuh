@@ -46,6 +46,13 @@ class KernelScope {
 // Device status word of the current device (set by bounded waits that ran out).
 int *device_status_ptr();
 
+// Stream-ordered workspace on the current device from a library-owned memory pool
+// whose freed memory stays mapped between calls (the device's default pool unmaps
+// freed memory at every synchronisation, and the next allocation maps it again).
+// Returns LINFORMER_OK or LINFORMER_ERR_ALLOC; free with workspace_free on a stream.
+int workspace_alloc(void **ptr, size_t bytes, cudaStream_t s);
+void workspace_free(void *ptr, cudaStream_t s);
+
 // Process-wide P.Vbar product-count setting (0 = automatic, 1 or 3).
 int pv_terms_setting();
 

@@ -31,6 +31,31 @@ constexpr int kMaxDevices = 64;
 int *g_status_addr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
+// One memory pool per device for workspaces, created on first use, kept for the
+// process (release threshold: unlimited, so freed memory stays mapped).
+cudaMemPool_t g_pools[kMaxDevices] = {};
+std::mutex g_pool_mu;
+
+cudaMemPool_t library_pool(int dev) {
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        uint64_t keep = ~uint64_t(0);
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pools[dev] = pool;
+    }
+    return g_pools[dev];
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape, enum and F rules shared by every entry point.
@@ -70,20 +95,52 @@ int run_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
     void *ws = nullptr;
     const size_t bytes = (size_t)p.units() * p.k * p.d * sizeof(float);
     if (!Kb) {
-        if (cudaMallocAsync(&ws, 2 * bytes, p.stream) != cudaSuccess) {
-            cudaGetLastError();
-            return LINFORMER_ERR_ALLOC;
-        }
+        if (workspace_alloc(&ws, 2 * bytes, p.stream) != LINFORMER_OK) return LINFORMER_ERR_ALLOC;
         Kb = static_cast<float *>(ws);
         Vb = reinterpret_cast<float *>(static_cast<char *>(ws) + bytes);
     }
     int st = simt_project(p, Kb, Vb);
     if (st == LINFORMER_OK && !Kbar_out) st = simt_attend(p, Kb, Vb);
-    if (ws) cudaFreeAsync(ws, p.stream);
+    if (ws) workspace_free(ws, p.stream);
     return st;
 }
 
 }  // namespace
+
+// Batch chunks of the host entry point's copy/compute pipeline.
+constexpr int kHostChunks = 4;
+
+// Two non-blocking streams per device for the host entry point's copies.
+cudaStream_t g_side[kMaxDevices][2] = {};
+std::mutex g_side_mu;
+
+cudaStream_t side_stream(int i) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    if (!g_side[dev][i] &&
+        cudaStreamCreateWithFlags(&g_side[dev][i], cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        g_side[dev][i] = nullptr;
+    }
+    return g_side[dev][i];
+}
+
+int workspace_alloc(void **ptr, size_t bytes, cudaStream_t s) {
+    int dev = 0;
+    cudaMemPool_t pool = nullptr;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) pool = library_pool(dev);
+    const cudaError_t e =
+        pool ? cudaMallocFromPoolAsync(ptr, bytes, pool, s) : cudaMallocAsync(ptr, bytes, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *ptr = nullptr;
+        return LINFORMER_ERR_ALLOC;
+    }
+    return LINFORMER_OK;
+}
+
+void workspace_free(void *ptr, cudaStream_t s) { cudaFreeAsync(ptr, s); }  // back to its pool
 
 KernelScope::KernelScope(int kernel_id, cudaStream_t s) : id_(kernel_id), s_(s) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -177,31 +234,78 @@ extern "C" int linformer_attn_fwd_host(const void *Q, const void *K, const void 
     const size_t total = 3 * up(qkv) + up(proj) * (distinct ? 2 : 1) + up(obytes) + up(pbytes);
     cudaStream_t s = as_stream(stream);
     char *base = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&base), total, s) != cudaSuccess) {
-        cudaGetLastError();
+    if (workspace_alloc(reinterpret_cast<void **>(&base), total, s) != LINFORMER_OK)
         return LINFORMER_ERR_ALLOC;
-    }
     char *dQ = base, *dK = dQ + up(qkv), *dV = dK + up(qkv), *dE = dV + up(qkv);
     char *dF = distinct ? dE + up(proj) : nullptr;
     char *dO = (distinct ? dF : dE) + up(proj);
     char *dP = pad_lengths ? dO + up(obytes) : nullptr;
-    bool ok = cudaMemcpyAsync(dQ, Q, qkv, cudaMemcpyHostToDevice, s) == cudaSuccess &&
-              cudaMemcpyAsync(dK, K, qkv, cudaMemcpyHostToDevice, s) == cudaSuccess &&
-              cudaMemcpyAsync(dV, V, qkv, cudaMemcpyHostToDevice, s) == cudaSuccess &&
-              cudaMemcpyAsync(dE, E, proj, cudaMemcpyHostToDevice, s) == cudaSuccess &&
-              (!dF || cudaMemcpyAsync(dF, F, proj, cudaMemcpyHostToDevice, s) == cudaSuccess) &&
-              (!dP || cudaMemcpyAsync(dP, pad_lengths, pbytes, cudaMemcpyHostToDevice, s) ==
-                          cudaSuccess);
+    // A pipeline over batch chunks: inputs come in on one side stream, each chunk's
+    // forward runs on `s` once its inputs are in, and its O goes out on the other
+    // side stream while later chunks compute (the two copy directions overlap).
+    // Events made for this call carry every dependency.
+    const size_t qrow = qkv / b, orow = obytes / b;  // bytes of one batch entry
+    // Chunk boundaries keep the kernels' 16-byte alignment only if a batch entry does.
+    const int chunks = (qrow % 256 || orow % 256) ? 1 : (b < kHostChunks ? b : kHostChunks);
+    cudaStream_t in = side_stream(0), out = side_stream(1);
+    cudaEvent_t ev[2 * kHostChunks + 2] = {};
+    const int nev = 2 * chunks + 2;
+    bool ok = in && out;
+    for (int i = 0; i < nev && ok; ++i)
+        ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventRecord(ev[0], s) == cudaSuccess &&  // after the allocation
+         cudaStreamWaitEvent(in, ev[0], 0) == cudaSuccess &&
+         cudaMemcpyAsync(dE, E, proj, cudaMemcpyHostToDevice, in) == cudaSuccess &&
+         (!dF || cudaMemcpyAsync(dF, F, proj, cudaMemcpyHostToDevice, in) == cudaSuccess) &&
+         (!dP || cudaMemcpyAsync(dP, pad_lengths, pbytes, cudaMemcpyHostToDevice, in) ==
+                     cudaSuccess);
     st = ok ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
-    if (st == LINFORMER_OK) {
-        Problem p{dQ, dK, dV, dE, dF, reinterpret_cast<const int32_t *>(dP), dO, b, h, n, d,
-                  k, share_mode, dtype, s};
+    for (int c = 0; c < chunks && st == LINFORMER_OK; ++c) {
+        const int b0 = (int)((int64_t)b * c / chunks), b1 = (int)((int64_t)b * (c + 1) / chunks);
+        const size_t off = qrow * b0, len = qrow * (b1 - b0);
+        cudaEvent_t inputs = ev[1 + 2 * c], done = ev[2 + 2 * c];
+        ok = cudaMemcpyAsync(dQ + off, static_cast<const char *>(Q) + off, len,
+                             cudaMemcpyHostToDevice, in) == cudaSuccess &&
+             cudaMemcpyAsync(dK + off, static_cast<const char *>(K) + off, len,
+                             cudaMemcpyHostToDevice, in) == cudaSuccess &&
+             cudaMemcpyAsync(dV + off, static_cast<const char *>(V) + off, len,
+                             cudaMemcpyHostToDevice, in) == cudaSuccess &&
+             cudaEventRecord(inputs, in) == cudaSuccess &&
+             cudaStreamWaitEvent(s, inputs, 0) == cudaSuccess;
+        if (!ok) {
+            st = LINFORMER_ERR_LAUNCH;
+            break;
+        }
+        Problem p{dQ + off, dK + off, dV + off, dE, dF,
+                  dP ? reinterpret_cast<const int32_t *>(dP) + b0 : nullptr, dO + orow * b0,
+                  b1 - b0, h, n, d, k, share_mode, dtype, s};
         st = run_forward(p, nullptr, nullptr);
+        if (st == LINFORMER_OK &&
+            !(cudaEventRecord(done, s) == cudaSuccess &&
+              cudaStreamWaitEvent(out, done, 0) == cudaSuccess &&
+              cudaMemcpyAsync(static_cast<char *>(O) + orow * b0, dO + orow * b0,
+                              orow * (b1 - b0), cudaMemcpyDeviceToHost, out) == cudaSuccess))
+            st = LINFORMER_ERR_LAUNCH;
     }
-    if (st == LINFORMER_OK &&
-        cudaMemcpyAsync(O, dO, obytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        st = LINFORMER_ERR_LAUNCH;
-    cudaFreeAsync(base, s);
+    // `s` goes on (and frees the workspace) only after both side streams are done.
+    const bool joined = in && out && ev[nev - 1] &&
+                        cudaEventRecord(ev[nev - 1], out) == cudaSuccess &&
+                        cudaStreamWaitEvent(s, ev[nev - 1], 0) == cudaSuccess;
+    cudaEvent_t in_done = nullptr;
+    const bool joined_in = in && cudaEventCreateWithFlags(&in_done, cudaEventDisableTiming) ==
+                                     cudaSuccess &&
+                           cudaEventRecord(in_done, in) == cudaSuccess &&
+                           cudaStreamWaitEvent(s, in_done, 0) == cudaSuccess;
+    if (in_done) cudaEventDestroy(in_done);
+    for (int i = 0; i < nev; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);  // released once the stream work is done
+    if (!joined || !joined_in) {  // queued copies must end before the free below
+        cudaGetLastError();
+        if (in) cudaStreamSynchronize(in);
+        if (out) cudaStreamSynchronize(out);
+        if (st == LINFORMER_OK) st = LINFORMER_ERR_LAUNCH;
+    }
+    workspace_free(base, s);
     if (cudaStreamSynchronize(s) != cudaSuccess && st == LINFORMER_OK) st = LINFORMER_ERR_LAUNCH;
     return st;
 }

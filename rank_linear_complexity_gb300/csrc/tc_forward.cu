@@ -88,11 +88,9 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
     const size_t part = up256(partial_bytes(units, C, mhalves));
     const size_t cnt = up256((units + 1) * sizeof(int));
     char *ws = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&ws), img + part + 2 * cnt, p.stream) !=
-        cudaSuccess) {
-        cudaGetLastError();
+    if (workspace_alloc(reinterpret_cast<void **>(&ws), img + part + 2 * cnt, p.stream) !=
+        LINFORMER_OK)
         return LINFORMER_ERR_ALLOC;
-    }
     uint8_t *images = reinterpret_cast<uint8_t *>(ws);
     float *partial = C > 1 ? reinterpret_cast<float *>(ws + img) : nullptr;
     int *counters = reinterpret_cast<int *>(ws + img + part);
@@ -174,7 +172,7 @@ int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
             st = launch_attend(tQ, tO, ap, grid, p.stream);
         }
     }
-    cudaFreeAsync(ws, p.stream);
+    workspace_free(ws, p.stream);
     return st;
 }
 

@@ -147,13 +147,16 @@ def test_projection_entry_point(mode):
         assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max() + 1e-6
 
 
-def test_host_entry_point_matches_device():
-    x = case_inputs(2, 2, 512, 64, 128, KV, BF16, seed=30)
-    O_dev = run(x, KV, BF16)
+@pytest.mark.parametrize("b,n,d,dtype,ragged", [(2, 512, 64, BF16, False),   # two chunks
+                                                 (5, 512, 64, BF16, True),    # uneven chunks
+                                                 (3, 130, 40, F32, False)])   # one chunk (rows
+def test_host_entry_point_matches_device(b, n, d, dtype, ragged):          # not 256-B multiples)
+    x = case_inputs(b, 2, n, d, 128, KV, dtype, ragged=ragged, seed=30 + b)
+    O_dev = run(x, KV, dtype)
     pin = {kk: (v.pin_memory() if v is not None else None) for kk, v in x.items()}
-    O_host = torch.empty(O_dev.shape, dtype=torch.bfloat16).pin_memory()
-    st = lf.linformer_attn_fwd_host(pin["Q"], pin["K"], pin["V"], pin["E"], None, None, O_host,
-                                    2, 2, 512, 64, 128, KV, BF16)
+    O_host = torch.empty(O_dev.shape, dtype=O_dev.dtype).pin_memory()
+    st = lf.linformer_attn_fwd_host(pin["Q"], pin["K"], pin["V"], pin["E"], None,
+                                    pin["lengths"], O_host, b, 2, n, d, 128, KV, dtype)
     assert st == 0, lf.status_string(st)
     assert torch.equal(O_host, O_dev.cpu())
 

@@ -108,7 +108,7 @@ int run_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
 }  // namespace
 
 // Batch chunks of the host entry point's copy/compute pipeline.
-constexpr int kHostChunks = 4;
+constexpr int kHostChunks = 8;
 
 // Two non-blocking streams per device for the host entry point's copies.
 cudaStream_t g_side[kMaxDevices][2] = {};

@@ -448,6 +448,91 @@ def run_approx_error(args):
     return 0
 
 
+BWD_SHAPE = dict(b=16, h=12, n=4096, d=64, k=256, share_mode=3)  # LAYERWISE
+
+
+def bwd_flop(b, h, n, d, k, **_):
+    """Algorithmic FLOPs of the backward: eleven n x k x d products per unit (Kbar, Vbar
+    recomputed; S, dP, dVbar, dQ, dKbar, dK, dV and the E and F terms), 2 FLOPs each."""
+    return 22.0 * b * h * n * k * d
+
+
+def run_backward(args):
+    """fp32 backward (linformer_attn_bwd) at n=4096, k=256, one shared projection."""
+    import rank_linear_complexity_gb300.linformer as lf
+    from rank_linear_complexity_gb300 import build as libbuild
+    from rank_linear_complexity_gb300.workloads import make_inputs, output_gradient
+    libbuild.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    c = BWD_SHAPE
+    b, h, n, d, k, mode = c["b"], c["h"], c["n"], c["d"], c["k"], c["share_mode"]
+    x = make_inputs(b, h, n, d, k, mode, 0, seed=77)
+    dO_h = output_gradient(b, h, n, d, seed=78)
+    g = {kk: (v.to(dev) if v is not None else None) for kk, v in x.items()}
+    dO = dO_h.to(dev)
+    dQ, dK, dV = torch.empty_like(g["Q"]), torch.empty_like(g["K"]), torch.empty_like(g["V"])
+    dE = torch.empty_like(g["E"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        st = lf.linformer_attn_bwd(g["Q"], g["K"], g["V"], g["E"], None, g["lengths"], dO, dQ,
+                                   dK, dV, dE, None, b, h, n, d, k, mode, 0, stream)
+        if st != 0:
+            raise lf.LinformerError(st, "linformer_attn_bwd")
+
+    steps = max(1, min(args.steps, 50))
+    sampler = ClockSampler(0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches0 = lf.linformer_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = lf.linformer_launch_count() - launches0
+    if lf.linformer_debug_read_device_status(stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+    ms_step = ev0.elapsed_time(ev1) / steps
+    tokens = b * h * n
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = clocks.get("sm_max_mhz") or 2070.0
+    peak = sms * 128 * 2 * max_mhz * 1e6 / 1e12  # fp32 FMA lanes x 2 FLOPs x clock
+    achieved = bwd_flop(**c) / (ms_step * 1e-3) / 1e12
+
+    # the oracle on a bounded sample of the same workload (units of one batch row)
+    from oracle import backward as bw
+    units = min(h, 12)
+    t0 = time.perf_counter()
+    bw.linformer_bwd(x["Q"][:1, :units], x["K"][:1, :units], x["V"][:1, :units], x["E"], None,
+                     None, dO_h[:1, :units], mode)
+    cpu_s = time.perf_counter() - t0
+    line = {
+        "experiment": "backward", "metric": "Linformer attn bwd Mtokens/s at n=4096,k=256 fp32",
+        "value": tokens / (ms_step * 1e-3) / 1e6, "unit": UNIT, "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "bwd_b16_h12_n4096_d64_k256_layerwise", **c,
+                   "l2": "inputs larger than L2 (805 MB of Q, K, V, dO)"},
+        "roofline": {"kernel": "backward (all launches)", "bound": "alu",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": f"derived: {sms} SMs x 128 fp32 lanes x 2 x {max_mhz} MHz"},
+        "gpu_launches": launches,
+        "clocks": {kk: clocks.get(kk) for kk in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "cpu_baseline": {"value": units * n / cpu_s / 1e6, "unit": UNIT,
+                         "cores": host_cores(), "kind": "oracle",
+                         "sample": f"{units} of {b * h} units, fp64 numpy oracle"},
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,10 +552,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--approx-error", action="store_true",
                     help="report the method's approximation error over n and k instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the fp32 backward at n=4096, k=256 instead")
     args = ap.parse_args()
     if args.approx_error:
         return run_approx_error(args)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
+    if args.backward:
+        return run_backward(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -108,7 +108,8 @@ typedef enum {
     LINFORMER_KERNEL_PROJECT_SIMT = 2,
     LINFORMER_KERNEL_ATTEND_SIMT = 3,
     LINFORMER_KERNEL_WINDOW = 4,    /* linformer_window_projection */
-    LINFORMER_KERNEL_COUNT = 5
+    LINFORMER_KERNEL_BACKWARD = 5,  /* the kernels of linformer_attn_bwd */
+    LINFORMER_KERNEL_COUNT = 6
 } linformer_kernel_id;
 
 /*
@@ -175,6 +176,25 @@ LINFORMER_API int linformer_attn_fwd_noalloc(const void *Q, const void *K, const
                                              const int32_t *pad_lengths, void *O,
                                              int b, int h, int n, int d, int k,
                                              int share_mode, int dtype, void *stream);
+
+/*
+ * The backward of linformer_attn_fwd: given dO = dLoss/dO, writes dQ, dK, dV
+ * ([b][h][n][d]) and dE (shaped like E) and, in PER_HEAD and HEADWISE modes, dF
+ * (shaped like F; in KV and LAYERWISE modes F is E and dE holds both terms, dF must be
+ * NULL).  The chain rule through the forward's definition (요약 설명, section Model):
+ * rows t >= L of K and V and query rows i >= L take no part (their gradients are
+ * zero), and the gradient of a shared E or F sums the terms of every unit that shares
+ * it.  fp32 only (LINFORMER_F32; other dtypes return LINFORMER_ERR_UNSUPPORTED),
+ * d <= 128, k <= 1024, b*h <= 65535 (else LINFORMER_ERR_SIZE).  All pointers are
+ * device pointers, 16-byte aligned; the caller owns every buffer; a stream-ordered
+ * workspace of b*h*(2 n k + k n + 4 k d) floats (plus b*h*k*n with a distinct F)
+ * comes from the library's pool and is returned to it in stream order.
+ */
+LINFORMER_API int linformer_attn_bwd(const void *Q, const void *K, const void *V,
+                                     const void *E, const void *F, const int32_t *pad_lengths,
+                                     const void *dO, void *dQ, void *dK, void *dV, void *dE,
+                                     void *dF, int b, int h, int n, int d, int k,
+                                     int share_mode, int dtype, void *stream);
 
 /*
  * Pooling or convolution instead of a learned projection (요약 설명, section

@@ -60,6 +60,10 @@ int pv_terms_setting();
 int simt_project(const Problem &p, float *Kbar, float *Vbar);
 int simt_attend(const Problem &p, const float *Kbar, const float *Vbar);
 
+// fp32 backward (simt_backward.cu).
+int simt_backward(const Problem &p, const float *dO, float *dQ, float *dK, float *dV, float *dE,
+                  float *dF);
+
 // Tensor-core kernels (tc_project.cu, tc_attend.cu).
 bool tc_supported(int n, int d, int k, int dtype);
 int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out);

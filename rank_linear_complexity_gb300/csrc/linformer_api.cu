@@ -211,6 +211,30 @@ extern "C" int linformer_project_fwd(const void *K, const void *V, const void *E
     return run_forward(p, Kbar, Vbar);
 }
 
+extern "C" int linformer_attn_bwd(const void *Q, const void *K, const void *V, const void *E,
+                                  const void *F, const int32_t *pad_lengths, const void *dO,
+                                  void *dQ, void *dK, void *dV, void *dE, void *dF, int b, int h,
+                                  int n, int d, int k, int share_mode, int dtype, void *stream) {
+    if (!Q || !K || !V || !E || !dO || !dQ || !dK || !dV || !dE) return LINFORMER_ERR_NULL;
+    int st = validate_common(b, h, n, d, k, share_mode, dtype);
+    if (st) return st;
+    if ((st = validate_f(share_mode, E, F))) return st;
+    if (dtype != LINFORMER_F32) return LINFORMER_ERR_UNSUPPORTED;
+    const bool distinct = share_mode == LINFORMER_SHARE_PER_HEAD ||
+                          share_mode == LINFORMER_SHARE_HEADWISE;
+    if (distinct != (dF != nullptr)) return distinct ? LINFORMER_ERR_NULL : LINFORMER_ERR_F_MODE;
+    const void *ptrs[] = {Q, K, V, E, F, dO, dQ, dK, dV, dE, dF};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return LINFORMER_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(pad_lengths) & 3u) return LINFORMER_ERR_ALIGN;
+    if ((int64_t)b * h > 65535) return LINFORMER_ERR_SIZE;
+    Problem p{Q, K, V, E, F, pad_lengths, nullptr, b, h, n, d, k, share_mode, dtype,
+              as_stream(stream)};
+    return simt_backward(p, static_cast<const float *>(dO), static_cast<float *>(dQ),
+                         static_cast<float *>(dK), static_cast<float *>(dV),
+                         static_cast<float *>(dE), static_cast<float *>(dF));
+}
+
 extern "C" int linformer_attn_fwd_host(const void *Q, const void *K, const void *V,
                                        const void *E, const void *F,
                                        const int32_t *pad_lengths, void *O, int b, int h,
@@ -381,6 +405,6 @@ extern "C" int linformer_profile_collect(double *ms, int64_t *launches) {
 extern "C" const char *linformer_kernel_name(int id) {
     static const char *names[LINFORMER_KERNEL_COUNT] = {
         "tc_project_kernel", "tc_attend_kernel", "simt_project_kernel", "simt_attend_kernel",
-        "window_projection_kernel"};
+        "window_projection_kernel", "backward_kernels"};
     return (id >= 0 && id < LINFORMER_KERNEL_COUNT) ? names[id] : nullptr;
 }

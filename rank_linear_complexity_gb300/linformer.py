@@ -17,7 +17,7 @@ from . import build as _build
 PER_HEAD, KV, HEADWISE, LAYERWISE = 0, 1, 2, 3
 F32, BF16, BF16_F32OUT = 0, 1, 2
 PATH_SIMT, PATH_TENSOR = 0, 1
-KERNEL_COUNT = 5
+KERNEL_COUNT = 6
 
 _lock = threading.Lock()
 _lib = None
@@ -30,7 +30,7 @@ SYMBOLS = [
     "linformer_select_path", "linformer_status_string", "linformer_debug_read_device_status",
     "linformer_set_pv_terms", "linformer_launch_count", "linformer_profile_enable",
     "linformer_profile_collect", "linformer_kernel_name", "linformer_attn_fwd_noalloc",
-    "linformer_window_projection",
+    "linformer_window_projection", "linformer_attn_bwd",
 ]
 
 
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.linformer_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_double),
                                                     ctypes.POINTER(ctypes.c_int64)]
             L.linformer_profile_collect.restype = _i
+            L.linformer_attn_bwd.argtypes = [_vp] * 12 + [_i] * 7 + [_vp]
+            L.linformer_attn_bwd.restype = _i
             L.linformer_window_projection.argtypes = [_vp, _vp, _i, _i, _i, _vp]
             L.linformer_window_projection.restype = _i
             L.linformer_kernel_name.argtypes = [_i]
@@ -238,3 +240,26 @@ def window_projection(n: int, k: int, weights=None, dtype=None, device="cuda", s
     if st != 0:
         raise LinformerError(st, "linformer_window_projection")
     return P
+
+
+def linformer_attn_bwd(Q, K, V, E, F, pad_lengths, dO, dQ, dK, dV, dE, dF, b, h, n, d, k,
+                       share_mode, dtype, stream=None) -> int:
+    return lib().linformer_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(E), _ptr(F),
+                                    _ptr(pad_lengths), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                    _ptr(dE), _ptr(dF), b, h, n, d, k, share_mode, dtype,
+                                    _stream_handle(stream))
+
+
+def attention_backward(Q, K, V, E, F, lengths, dO, share_mode: int = PER_HEAD, stream=None):
+    """(dQ, dK, dV, dE, dF) of device fp32 tensors; dF is None when F is E (KV, LAYERWISE)."""
+    import torch
+    b, h, n, d, k = _dims(Q, E, share_mode)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    dE = torch.empty_like(E)
+    distinct = share_mode in (PER_HEAD, HEADWISE)
+    dF = torch.empty_like(F if F is not None else E) if distinct else None
+    st = linformer_attn_bwd(Q, K, V, E, F, lengths, dO, dQ, dK, dV, dE, dF, b, h, n, d, k,
+                            share_mode, dtype_code(Q), stream)
+    if st != 0:
+        raise LinformerError(st, "linformer_attn_bwd")
+    return dQ, dK, dV, dE, dF

@@ -109,3 +109,9 @@ def make_inputs(b: int, h: int, n: int, d: int, k: int, share_mode: int, dtype: 
 
 def workload_inputs(w: Workload) -> dict:
     return make_inputs(w.b, w.h, w.n, w.d, w.k, w.share_mode, w.dtype, w.ragged, w.seed)
+
+
+def output_gradient(b: int, h: int, n: int, d: int, seed: int = 4321) -> torch.Tensor:
+    """Seeded upstream gradient dLoss/dO for the backward: N(0, 1), fp32, on the CPU."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(b, h, n, d, generator=g, dtype=torch.float32)

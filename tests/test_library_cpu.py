@@ -100,3 +100,24 @@ def test_pv_terms_setting(L):
     assert lf.linformer_set_pv_terms(2) == prev
     assert lf.linformer_set_pv_terms(prev) == 2
     assert lf.linformer_set_pv_terms(4) == -4
+
+
+@pytest.mark.parametrize("args,expected", [
+    (dict(dO=None), -1),
+    (dict(dE=None), -1),
+    (dict(dF=None, share_mode=0), -1),          # PER_HEAD has a distinct F: dF required
+    (dict(share_mode=1), -6),                   # KV: F is E, so dF must be NULL
+    (dict(dtype=1), -3),                        # fp32 only
+    (dict(d=129), -3),
+    (dict(b=300, h=300), -2),                   # more than 65535 units
+    (dict(dQ=A + 8), -5),
+    (dict(share_mode=7), -4),
+])
+def test_backward_argument_errors_are_reported_before_launch(L, args, expected):
+    a = dict(Q=A, K=A, V=A, E=A, F=A + 4096, pad=None, dO=A, dQ=A, dK=A, dV=A, dE=A,
+             dF=A + 4096, b=2, h=3, n=64, d=64, k=32, share_mode=0, dtype=0)
+    a.update(args)
+    st = lf.linformer_attn_bwd(a["Q"], a["K"], a["V"], a["E"], a["F"], a["pad"], a["dO"],
+                               a["dQ"], a["dK"], a["dV"], a["dE"], a["dF"], a["b"], a["h"],
+                               a["n"], a["d"], a["k"], a["share_mode"], a["dtype"], stream=0)
+    assert st == expected, lf.status_string(st)

@@ -533,6 +533,92 @@ def run_backward(args):
     return 0
 
 
+# The pages' single-GPU inference table: (n, k) pairs, RoBERTa-base heads (h = 12, d = 64).
+TABLE_POINTS = [(512, 128), (4096, 128), (4096, 256), (65536, 128), (65536, 256)]
+TABLE_H, TABLE_D = 12, 64
+V100_BYTES = 16e9  # the pages' GPU capacity
+
+
+def time_call(fn, steps, warmup, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_inference_table(args):
+    """Time and largest batch of Linformer attention against dense softmax attention
+    (attention only, one layer, h = 12, d = 64), at the pages' (n, k) points.  Memory per
+    sequence = its Q, K, V, O plus the workspace the call draws from the library pool
+    (measured high-water mark ÷ sequences); the largest batch is what fits in a capacity
+    after E and F; memory saving = ratio of largest batches, as the pages define it."""
+    import rank_linear_complexity_gb300.linformer as lf
+    from rank_linear_complexity_gb300 import build as libbuild
+    from rank_linear_complexity_gb300.workloads import make_inputs
+    libbuild.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm = torch.cuda.get_device_properties(dev).total_memory
+    h, d = TABLE_H, TABLE_D
+    rows = []
+
+    def measure(fn, seqs, io_bytes_per_seq, fixed_bytes, steps):
+        torch.cuda.synchronize()
+        lf.linformer_pool_peak_bytes(reset=True)
+        fn()
+        torch.cuda.synchronize()
+        ws = lf.linformer_pool_peak_bytes()
+        ms = time_call(fn, steps, 2, stream)
+        per_seq = io_bytes_per_seq + ws / seqs
+        return {"ms_per_seq": ms / seqs, "bytes_per_seq": per_seq,
+                "max_batch_16GB": int(max(0, V100_BYTES - fixed_bytes) // per_seq),
+                "max_batch_hbm": int(max(0, hbm - fixed_bytes) // per_seq)}
+
+    for n, k in TABLE_POINTS:
+        row = {"n": n, "k": k}
+        # dense fp32: the n x n scores of every unit; one head at n = 65536 (17 GB)
+        bd, hd = (16, h) if n <= 512 else ((1, h) if n <= 4096 else (1, 1))
+        x = make_inputs(bd, hd, n, d, 1, 0, 0, seed=n)
+        Q, K, V = (x[c].to(dev) for c in "QKV")
+        O = torch.empty_like(Q)
+        seqs = bd * hd / h
+        fn = lambda: lf.dense_attention(Q, K, V, out=O)
+        row["dense_f32"] = measure(fn, seqs, 4 * h * n * d * 4, 0, 3 if n > 4096 else 10)
+        del Q, K, V, O, x
+        # Linformer, one E = F shared by all heads (layerwise), fp32 and bf16 inputs
+        bl = 16 if n <= 4096 else 1
+        for name, dt in (("linformer_f32", 0), ("linformer_bf16", 1)):
+            x = make_inputs(bl, h, n, d, k, 3, dt, seed=n + k)
+            g = {c: (v.to(dev) if v is not None else None) for c, v in x.items()}
+            O = torch.empty_like(g["Q"])
+            es = 4 if dt == 0 else 2
+            fn = lambda: lf.attention(g["Q"], g["K"], g["V"], g["E"], None, None, 3, out=O)
+            row[name] = measure(fn, bl, 4 * h * n * d * es, k * n * es, 10)
+            del g, O, x
+        for name in ("linformer_f32", "linformer_bf16"):
+            row[name]["speedup_vs_dense_f32"] = (row["dense_f32"]["ms_per_seq"] /
+                                                 row[name]["ms_per_seq"])
+            for cap in ("16GB", "hbm"):
+                den = row["dense_f32"][f"max_batch_{cap}"]
+                row[name][f"memory_saving_{cap}"] = (row[name][f"max_batch_{cap}"] / den
+                                                     if den else None)
+        rows.append(row)
+        torch.cuda.empty_cache()
+    print(json.dumps({"experiment": "inference_table", "h": h, "d": d,
+                      "share_mode": "layerwise (one E = F)", "hbm_bytes": hbm,
+                      "note": "attention only, one layer; dense keeps the n x n scores of "
+                              "every head in device memory; ms per sequence of 12 heads",
+                      "rows": rows}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -554,9 +640,13 @@ def main():
                     help="report the method's approximation error over n and k instead")
     ap.add_argument("--backward", action="store_true",
                     help="time the fp32 backward at n=4096, k=256 instead")
+    ap.add_argument("--inference-table", action="store_true",
+                    help="Linformer against dense attention: time and largest batch")
     args = ap.parse_args()
     if args.approx_error:
         return run_approx_error(args)
+    if args.inference_table:
+        return run_inference_table(args)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
     if args.backward:
         return run_backward(args)

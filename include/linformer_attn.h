@@ -109,7 +109,8 @@ typedef enum {
     LINFORMER_KERNEL_ATTEND_SIMT = 3,
     LINFORMER_KERNEL_WINDOW = 4,    /* linformer_window_projection */
     LINFORMER_KERNEL_BACKWARD = 5,  /* the kernels of linformer_attn_bwd */
-    LINFORMER_KERNEL_COUNT = 6
+    LINFORMER_KERNEL_DENSE = 6,     /* the kernels of linformer_dense_attn_fwd */
+    LINFORMER_KERNEL_COUNT = 7
 } linformer_kernel_id;
 
 /*
@@ -195,6 +196,27 @@ LINFORMER_API int linformer_attn_bwd(const void *Q, const void *K, const void *V
                                      const void *dO, void *dQ, void *dK, void *dV, void *dE,
                                      void *dF, int b, int h, int n, int d, int k,
                                      int share_mode, int dtype, void *stream);
+
+/*
+ * Dense softmax attention, the full-attention baseline that the pages' inference table
+ * ("Linformer 요약 설명", section Inference-time Efficiency Results) compares the
+ * method with: O = softmax(Q K^T / sqrt(d)) V per unit, Q, K, V, O [b][h][n][d] fp32.
+ * With pad_lengths, keys t >= L take no part in the softmax and query rows i >= L are
+ * written as zero.  The n x n scores of every unit live in a stream-ordered workspace
+ * of b*h*n*n floats from the library's pool (the memory the standard form needs).
+ * fp32 only (else LINFORMER_ERR_UNSUPPORTED); d <= 128; b*h <= 65535 and n <= 8388480
+ * (else LINFORMER_ERR_SIZE); pointers device, 16-byte aligned; the caller owns them.
+ */
+LINFORMER_API int linformer_dense_attn_fwd(const void *Q, const void *K, const void *V,
+                                           const int32_t *pad_lengths, void *O, int b, int h,
+                                           int n, int d, int dtype, void *stream);
+
+/*
+ * Largest number of bytes the library's workspace pool on the current device has had
+ * in use at once since the pool was created or last reset; reset != 0 then sets the
+ * mark back to the bytes in use now.  Returns -1 if the pool cannot be queried.
+ */
+LINFORMER_API int64_t linformer_pool_peak_bytes(int reset);
 
 /*
  * Pooling or convolution instead of a learned projection (요약 설명, section

@@ -24,19 +24,22 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def dense_fwd(Q, K, V, pad_lengths=None):
-    """O [b][h][n][d] in float64."""
+def dense_fwd(Q, K, V, pad_lengths=None, rows=None):
+    """O [b][h][n][d] in float64; with `rows` (query row indices) only those rows,
+    O [b][h][len(rows)][d] (each row of the definition stands alone)."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     b, h, n, d = Q.shape
     pad = None if pad_lengths is None else np.asarray(_f64(pad_lengths)).astype(np.int64)
-    O = np.zeros_like(Q)
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    O = np.zeros((b, h, len(rows), d))
     for bi in range(b):
         L = n if pad is None else int(min(max(pad[bi], 0), n))
-        if L == 0:
+        live = np.nonzero(rows < L)[0]                           # rows i >= L stay 0
+        if L == 0 or live.size == 0:
             continue
         for hi in range(h):
-            S = (Q[bi, hi, :L] @ K[bi, hi, :L].T) / np.sqrt(d)    # L x L, valid keys only
+            S = (Q[bi, hi, rows[live]] @ K[bi, hi, :L].T) / np.sqrt(d)  # valid keys only
             P = np.exp(S - S.max(axis=1, keepdims=True))
             P /= P.sum(axis=1, keepdims=True)
-            O[bi, hi, :L] = P @ V[bi, hi, :L]
+            O[bi, hi, live] = P @ V[bi, hi, :L]
     return O

@@ -60,6 +60,9 @@ int pv_terms_setting();
 int simt_project(const Problem &p, float *Kbar, float *Vbar);
 int simt_attend(const Problem &p, const float *Kbar, const float *Vbar);
 
+// fp32 dense softmax attention (simt_dense.cu).
+int simt_dense_attention(const Problem &p);
+
 // fp32 backward (simt_backward.cu).
 int simt_backward(const Problem &p, const float *dO, float *dQ, float *dK, float *dV, float *dE,
                   float *dF);

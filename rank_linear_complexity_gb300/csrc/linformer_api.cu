@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/linformer_attn.h: argument
 // validation, path selection, stream-ordered workspace, launch bookkeeping,
 // profiling events and the device status word.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -8,6 +9,7 @@
 #include <vector>
 
 #include "internal.cuh"
+#include "simt_gemm.cuh"
 
 namespace linformer {
 
@@ -94,13 +96,27 @@ int run_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
     float *Kb = Kbar_out, *Vb = Vbar_out;
     void *ws = nullptr;
     const size_t bytes = (size_t)p.units() * p.k * p.d * sizeof(float);
+    // fp32 inputs: the SIMT matrix-product kernel (split projections, then scores,
+    // row softmax and P Vbar; the partials and P share the space after Kbar and Vbar);
+    // bf16 inputs: the fused SIMT projection and attention kernels
+    const bool f32 = p.dtype == LINFORMER_F32;
+    const size_t scores = Kbar_out ? 0 : (size_t)p.units() * p.n * p.k * sizeof(float);
+    const size_t part = f32 ? std::max((size_t)simt::kMaxSplits * bytes, scores) : 0;
+    const size_t need = (Kb ? 0 : 2 * bytes) + part;
+    if (need && workspace_alloc(&ws, need, p.stream) != LINFORMER_OK) return LINFORMER_ERR_ALLOC;
+    char *wp = static_cast<char *>(ws);
     if (!Kb) {
-        if (workspace_alloc(&ws, 2 * bytes, p.stream) != LINFORMER_OK) return LINFORMER_ERR_ALLOC;
-        Kb = static_cast<float *>(ws);
-        Vb = reinterpret_cast<float *>(static_cast<char *>(ws) + bytes);
+        Kb = reinterpret_cast<float *>(wp);
+        Vb = reinterpret_cast<float *>(wp + bytes);
+        wp += 2 * bytes;
     }
-    int st = simt_project(p, Kb, Vb);
-    if (st == LINFORMER_OK && !Kbar_out) st = simt_attend(p, Kb, Vb);
+    int st = f32 ? simt::project_f32(p, Kb, Vb, reinterpret_cast<float *>(wp),
+                                     LINFORMER_KERNEL_PROJECT_SIMT)
+                 : simt_project(p, Kb, Vb);
+    if (st == LINFORMER_OK && !Kbar_out)
+        st = f32 ? simt::attend_f32(p, Kb, Vb, reinterpret_cast<float *>(wp),
+                                    LINFORMER_KERNEL_ATTEND_SIMT)
+                 : simt_attend(p, Kb, Vb);
     if (ws) workspace_free(ws, p.stream);
     return st;
 }
@@ -233,6 +249,40 @@ extern "C" int linformer_attn_bwd(const void *Q, const void *K, const void *V, c
     return simt_backward(p, static_cast<const float *>(dO), static_cast<float *>(dQ),
                          static_cast<float *>(dK), static_cast<float *>(dV),
                          static_cast<float *>(dE), static_cast<float *>(dF));
+}
+
+extern "C" int linformer_dense_attn_fwd(const void *Q, const void *K, const void *V,
+                                        const int32_t *pad_lengths, void *O, int b, int h, int n,
+                                        int d, int dtype, void *stream) {
+    if (!Q || !K || !V || !O) return LINFORMER_ERR_NULL;
+    int st = validate_common(b, h, n, d, 1, LINFORMER_SHARE_PER_HEAD, dtype);
+    if (st) return st;
+    if (dtype != LINFORMER_F32) return LINFORMER_ERR_UNSUPPORTED;
+    const void *ptrs[] = {Q, K, V, O};
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return LINFORMER_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(pad_lengths) & 3u) return LINFORMER_ERR_ALIGN;
+    if ((int64_t)b * h > 65535 || n > 65535 * 128) return LINFORMER_ERR_SIZE;
+    Problem p{Q, K, V, nullptr, nullptr, pad_lengths, O, b, h, n, d, 1, LINFORMER_SHARE_PER_HEAD,
+              dtype, as_stream(stream)};
+    return simt_dense_attention(p);
+}
+
+extern "C" int64_t linformer_pool_peak_bytes(int reset) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    cudaMemPool_t pool = library_pool(dev);
+    if (!pool) return -1;
+    uint64_t high = 0;
+    if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &high) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (reset) {
+        uint64_t zero = 0;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero);
+    }
+    return (int64_t)high;
 }
 
 extern "C" int linformer_attn_fwd_host(const void *Q, const void *K, const void *V,
@@ -405,6 +455,6 @@ extern "C" int linformer_profile_collect(double *ms, int64_t *launches) {
 extern "C" const char *linformer_kernel_name(int id) {
     static const char *names[LINFORMER_KERNEL_COUNT] = {
         "tc_project_kernel", "tc_attend_kernel", "simt_project_kernel", "simt_attend_kernel",
-        "window_projection_kernel", "backward_kernels"};
+        "window_projection_kernel", "backward_kernels", "dense_attention_kernels"};
     return (id >= 0 && id < LINFORMER_KERNEL_COUNT) ? names[id] : nullptr;
 }

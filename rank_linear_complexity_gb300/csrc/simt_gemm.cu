@@ -1,0 +1,339 @@
+// Batched fp32 SIMT matrix products and the row softmax (declared in simt_gemm.cuh).
+#include <algorithm>
+
+#include "simt_gemm.cuh"
+
+namespace linformer {
+namespace simt {
+namespace {
+
+constexpr int kBK = 16;        // depth of one product step
+constexpr int kThreads = 256;  // 16 x 16 threads, each owning (BM/16) x (BN/16) outputs
+
+__device__ __forceinline__ int unit_length(const int32_t *pad, int unit, int h, int n) {
+    if (!pad) return n;
+    const int L = pad[unit / h];
+    return L < 0 ? 0 : (L > n ? n : L);
+}
+
+// Register staging of one BX x kBK operand tile: BX / 16 elements per thread, taken as
+// groups of four along the contiguous axis (a group is wholly in or out of range
+// when vec is set: the contiguous extent is then a multiple of four).
+template <int BX>
+struct Stage {
+    static constexpr int kGroups = BX / 64;  // groups of four per thread
+    float v[kGroups][4];
+
+    __device__ __forceinline__ void load(const Operand &o, const float *m, int x0, int k0, int X,
+                                         int K, int L) {
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            const int idx = threadIdx.x + g * kThreads;
+            int x, kk;
+            if (o.xfast) {
+                x = x0 + (idx % (BX / 4)) * 4;
+                kk = k0 + idx / (BX / 4);
+            } else {
+                x = x0 + idx / (kBK / 4);
+                kk = k0 + (idx % (kBK / 4)) * 4;
+            }
+            if (o.vec) {
+                const bool in = x < X && kk < K;
+                float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (in) {
+                    const long long off = o.xfast ? (long long)kk * o.ld + x : (long long)x * o.ld + kk;
+                    q = __ldg(reinterpret_cast<const float4 *>(m + off));
+                }
+                v[g][0] = q.x;
+                v[g][1] = q.y;
+                v[g][2] = q.z;
+                v[g][3] = q.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int xe = o.xfast ? x + e : x, ke = o.xfast ? kk : kk + e;
+                    v[g][e] = (xe < X && ke < K)
+                                  ? __ldg(m + (o.xfast ? (long long)ke * o.ld + xe
+                                                       : (long long)xe * o.ld + ke))
+                                  : 0.f;
+                }
+            }
+            if (o.mask_x | o.mask_k) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int xe = o.xfast ? x + e : x, ke = o.xfast ? kk : kk + e;
+                    if ((o.mask_x && xe >= L) || (o.mask_k && ke >= L)) v[g][e] = 0.f;
+                }
+            }
+        }
+    }
+
+    // into s[kk][x] (row stride BX + 4)
+    __device__ __forceinline__ void store(const Operand &o, float *s) const {
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            const int idx = threadIdx.x + g * kThreads;
+            if (o.xfast) {
+                const int x = (idx % (BX / 4)) * 4, kk = idx / (BX / 4);
+                *reinterpret_cast<float4 *>(s + kk * (BX + 4) + x) =
+                    make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
+            } else {
+                const int x = idx / (kBK / 4), kk = (idx % (kBK / 4)) * 4;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[(kk + e) * (BX + 4) + x] = v[g][e];
+            }
+        }
+    }
+};
+
+// One BM x BN output tile of unit blockIdx.z per CTA.  Thread (tx, ty) owns rows
+// ty*4 + {0..3} (+ 64, + 128 ... for BM > 64) and columns tx*4 + {0..3} (+ 64 ...), so
+// its shared-memory reads are 16-byte loads that a warp serves in two passes.  The
+// next tile's global loads are in registers while the current one is multiplied.
+template <int BM, int BN>
+__global__ void __launch_bounds__(kThreads, 2) batched_gemm_kernel(const GemmArgs g) {
+    constexpr int TM = BM / 16, TN = BN / 16;
+    __shared__ __align__(16) float sA[2][kBK * (BM + 4)];
+    __shared__ __align__(16) float sB[2][kBK * (BN + 4)];
+    const int z = blockIdx.z, tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int tiles_n = gridDim.x / g.splits, split = blockIdx.x / tiles_n;
+    const int row0 = blockIdx.y * BM, col0 = (blockIdx.x % tiles_n) * BN;
+    const int kbeg = split * g.kchunk, kend = min(g.K, kbeg + g.kchunk);
+    const float *A = g.A.mat(z, g.h), *B = g.B.mat(z, g.h);
+    const int L = unit_length(g.pad, z, g.h, g.n);
+    Stage<BM> ra;
+    Stage<BN> rb;
+    float acc[TM][TN] = {};
+    ra.load(g.A, A, row0, kbeg, g.M, kend, L);
+    rb.load(g.B, B, col0, kbeg, g.N, kend, L);
+    ra.store(g.A, sA[0]);
+    rb.store(g.B, sB[0]);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = kbeg; k0 < kend; k0 += kBK) {
+        const bool more = k0 + kBK < kend;
+        if (more) {
+            ra.load(g.A, A, row0, k0 + kBK, g.M, kend, L);
+            rb.load(g.B, B, col0, k0 + kBK, g.N, kend, L);
+        }
+        const float *a_s = sA[buf], *b_s = sB[buf];
+#pragma unroll
+        for (int kk = 0; kk < kBK; ++kk) {
+            float a[TM], b[TN];
+#pragma unroll
+            for (int q = 0; q < TM / 4; ++q) {
+                const float4 t = *reinterpret_cast<const float4 *>(a_s + kk * (BM + 4) + q * 64 + ty * 4);
+                a[q * 4] = t.x;
+                a[q * 4 + 1] = t.y;
+                a[q * 4 + 2] = t.z;
+                a[q * 4 + 3] = t.w;
+            }
+#pragma unroll
+            for (int q = 0; q < TN / 4; ++q) {
+                const float4 t = *reinterpret_cast<const float4 *>(b_s + kk * (BN + 4) + q * 64 + tx * 4);
+                b[q * 4] = t.x;
+                b[q * 4 + 1] = t.y;
+                b[q * 4 + 2] = t.z;
+                b[q * 4 + 3] = t.w;
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        if (more) {
+            buf ^= 1;
+            ra.store(g.A, sA[buf]);
+            rb.store(g.B, sB[buf]);
+        }
+        __syncthreads();
+    }
+    if (g.splits > 1) {
+        float *Pt = g.part + ((long long)split * gridDim.z + z) * g.M * g.N;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int r = row0 + (i / 4) * 64 + ty * 4 + (i % 4);
+            if (r >= g.M) continue;
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const int c = col0 + (j / 4) * 64 + tx * 4 + (j % 4);
+                if (c < g.N) Pt[(long long)r * g.N + c] = g.alpha * acc[i][j];
+            }
+        }
+        return;
+    }
+    float *C = g.C + (long long)z * g.sC;
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int r = row0 + (i / 4) * 64 + ty * 4 + (i % 4);
+        if (r >= g.M) continue;
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int c = col0 + (j / 4) * 64 + tx * 4 + (j % 4);
+            if (c >= g.N) continue;
+            float v = g.alpha * acc[i][j];
+            if (g.beta != 0.f) v = fmaf(g.beta, C[(long long)r * g.ldc + c], v);
+            if ((g.mask_rows && r >= L) || (g.mask_cols && c >= L)) v = 0.f;
+            C[(long long)r * g.ldc + c] = v;
+        }
+    }
+}
+
+// C = sum over splits of part[split] (+ beta C), with the output masks, in split order.
+__global__ void splitk_reduce_kernel(const GemmArgs g, long long units) {
+    const long long mn = (long long)g.M * g.N;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= units * mn) return;
+    const int z = (int)(i / mn);
+    const long long e = i % mn;
+    const int r = (int)(e / g.N), c = (int)(e % g.N);
+    const int L = unit_length(g.pad, z, g.h, g.n);
+    float v = 0.f;
+    for (int sp = 0; sp < g.splits; ++sp) v += g.part[((long long)sp * units + z) * mn + e];
+    float *C = g.C + (long long)z * g.sC + (long long)r * g.ldc + c;
+    if (g.beta != 0.f) v = fmaf(g.beta, *C, v);
+    if ((g.mask_rows && r >= L) || (g.mask_cols && c >= L)) v = 0.f;
+    *C = v;
+}
+
+// Rows of S (units x rows_per_unit x cols, in place): softmax for rows i < L (over the
+// columns j < L when mask_cols), zero for i >= L.  One warp per row; the first pass
+// keeps a running maximum and a rescaled running sum, the second writes p.
+__global__ void softmax_rows_kernel(float *S, const int32_t *pad, int h, int rows_per_unit,
+                                    int cols, long long rows, int mask_cols) {
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const int z = (int)(row / rows_per_unit), i = (int)(row % rows_per_unit);
+    int L = pad ? pad[z / h] : rows_per_unit;
+    L = L < 0 ? 0 : (L > rows_per_unit ? rows_per_unit : L);
+    float *s = S + row * cols;
+    if (i >= L) {
+        for (int j = lane; j < cols; j += 32) s[j] = 0.f;
+        return;
+    }
+    const int live = mask_cols ? (L < cols ? L : cols) : cols;
+    float m = -INFINITY, l = 0.f;
+    for (int j = lane; j < live; j += 32) {
+        const float v = s[j];
+        if (v > m) {
+            l = l * expf(m - v) + 1.f;
+            m = v;
+        } else {
+            l += expf(v - m);
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+        const float lo = __shfl_xor_sync(0xffffffffu, l, o);
+        const float mn = fmaxf(m, mo);
+        l = (m == -INFINITY ? 0.f : l * expf(m - mn)) + (mo == -INFINITY ? 0.f : lo * expf(mo - mn));
+        m = mn;
+    }
+    const float inv = 1.f / l;
+    for (int j = lane; j < cols; j += 32) s[j] = j < live ? expf(s[j] - m) * inv : 0.f;
+}
+
+// Whether an operand's 4-element groups along its contiguous axis can be 16-byte
+// loads: aligned base, strides and ld, and a contiguous extent that is a multiple of 4.
+void set_vec(Operand &o, int contiguous_extent) {
+    o.vec = (reinterpret_cast<uintptr_t>(o.p) & 15u) == 0 && o.ld % 4 == 0 &&
+            (o.index == kShared || o.stride % 4 == 0) && contiguous_extent % 4 == 0;
+}
+
+template <int BM, int BN>
+int launch_gemm(const GemmArgs &g, int units, cudaStream_t s, int kernel_id) {
+    const long long gx = (long long)((g.N + BN - 1) / BN) * g.splits;
+    dim3 grid((unsigned)gx, (unsigned)((g.M + BM - 1) / BM), (unsigned)units);
+    if (gx > 0x7fffffffLL || grid.y > 65535u || grid.z > 65535u) return LINFORMER_ERR_SIZE;
+    {
+        KernelScope scope(kernel_id, s);
+        batched_gemm_kernel<BM, BN><<<grid, kThreads, 0, s>>>(g);
+    }
+    if (g.splits > 1) {
+        const long long total = (long long)units * g.M * g.N;
+        KernelScope scope(kernel_id, s);
+        splitk_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(g, units);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, int max_splits, int sms,
+                 int kernel_id) {
+    set_vec(g.A, g.A.xfast ? g.M : g.K);
+    set_vec(g.B, g.B.xfast ? g.N : g.K);
+    const int BM = g.M <= 64 ? 64 : 128, BN = (g.M <= 64 || g.N <= 64) ? 64 : 128;
+    g.splits = 1;
+    g.kchunk = (g.K + kBK - 1) / kBK * kBK;
+    g.part = part;
+    if (part && max_splits > 1) {
+        const long long ctas = (long long)((g.N + BN - 1) / BN) * ((g.M + BM - 1) / BM) * units;
+        long long want = (8LL * sms + ctas - 1) / ctas;
+        want = std::min<long long>(want, std::min<long long>(max_splits, std::max(1, g.K / 256)));
+        if (want > 1) {
+            const int chunk = (g.K + (int)want - 1) / (int)want;
+            g.kchunk = (chunk + kBK - 1) / kBK * kBK;
+            g.splits = (g.K + g.kchunk - 1) / g.kchunk;
+        }
+    }
+    if (BM == 64) return launch_gemm<64, 64>(g, units, s, kernel_id);
+    if (BN == 64) return launch_gemm<128, 64>(g, units, s, kernel_id);
+    return launch_gemm<128, 128>(g, units, s, kernel_id);
+}
+
+
+int softmax_rows(float *S, const int32_t *pad, int h, int rows_per_unit, int cols,
+                 long long units, int mask_cols, cudaStream_t s, int kernel_id) {
+    const long long rows = units * rows_per_unit;
+    const long long blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL) return LINFORMER_ERR_SIZE;
+    KernelScope scope(kernel_id, s);
+    softmax_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(S, pad, h, rows_per_unit, cols, rows,
+                                                       mask_cols);
+    return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
+}
+
+int project_f32(const Problem &p, float *Kbar, float *Vbar, float *part, int kernel_id) {
+    const int units = (int)p.units(), n = p.n, d = p.d, k = p.k;
+    const long long kd = (long long)k * d, nd = (long long)n * d, kn = (long long)k * n;
+    const int pidx = p.proj_per_head() ? kPerHead : kShared;
+    const int sms = sm_count();
+    const float *K = static_cast<const float *>(p.K), *V = static_cast<const float *>(p.V);
+    const float *E = static_cast<const float *>(p.E), *F = static_cast<const float *>(p.f_or_e());
+    GemmArgs g{opA(E, kn, n, 0, pidx), opB(K, nd, d, 0, kPerUnit, 1), Kbar, kd, d, k, d, n, 1.f,
+               0.f, p.pad, p.h, n, 0, 0, 1, 0, nullptr};
+    int st = batched_gemm(g, units, p.stream, part, kMaxSplits, sms, kernel_id);
+    if (st) return st;
+    g.A = opA(F, kn, n, 0, pidx);
+    g.B = opB(V, nd, d, 0, kPerUnit, 1);
+    g.C = Vbar;
+    return batched_gemm(g, units, p.stream, part, kMaxSplits, sms, kernel_id);
+}
+
+int attend_f32(const Problem &p, const float *Kbar, const float *Vbar, float *P,
+               int kernel_id) {
+    const int units = (int)p.units(), n = p.n, d = p.d, k = p.k;
+    const long long kd = (long long)k * d, nd = (long long)n * d, nk = (long long)n * k;
+    GemmArgs g{opA(static_cast<const float *>(p.Q), nd, d, 0, kPerUnit),
+               opB(Kbar, kd, d, 1, kPerUnit), P, nk, k, n, k, d, 1.f / sqrtf((float)d), 0.f,
+               p.pad, p.h, n, 0, 0, 1, 0, nullptr};
+    int st = batched_gemm(g, units, p.stream, nullptr, 1, 0, kernel_id);
+    if (!st) st = softmax_rows(P, p.pad, p.h, n, k, units, 0, p.stream, kernel_id);
+    if (st) return st;
+    g = GemmArgs{opA(P, nk, k, 0, kPerUnit), opB(Vbar, kd, d, 0, kPerUnit),
+                 static_cast<float *>(p.O), nd, d, n, d, k, 1.f, 0.f, p.pad, p.h, n, 1, 0,
+                 1, 0, nullptr};
+    return batched_gemm(g, units, p.stream, nullptr, 1, 0, kernel_id);
+}
+
+int sm_count() {
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 148;
+}
+
+}  // namespace simt
+}  // namespace linformer

@@ -17,7 +17,7 @@ from . import build as _build
 PER_HEAD, KV, HEADWISE, LAYERWISE = 0, 1, 2, 3
 F32, BF16, BF16_F32OUT = 0, 1, 2
 PATH_SIMT, PATH_TENSOR = 0, 1
-KERNEL_COUNT = 6
+KERNEL_COUNT = 7
 
 _lock = threading.Lock()
 _lib = None
@@ -30,7 +30,8 @@ SYMBOLS = [
     "linformer_select_path", "linformer_status_string", "linformer_debug_read_device_status",
     "linformer_set_pv_terms", "linformer_launch_count", "linformer_profile_enable",
     "linformer_profile_collect", "linformer_kernel_name", "linformer_attn_fwd_noalloc",
-    "linformer_window_projection", "linformer_attn_bwd",
+    "linformer_window_projection", "linformer_attn_bwd", "linformer_dense_attn_fwd",
+    "linformer_pool_peak_bytes",
 ]
 
 
@@ -79,6 +80,10 @@ def lib() -> ctypes.CDLL:
             L.linformer_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_double),
                                                     ctypes.POINTER(ctypes.c_int64)]
             L.linformer_profile_collect.restype = _i
+            L.linformer_dense_attn_fwd.argtypes = [_vp] * 5 + [_i] * 5 + [_vp]
+            L.linformer_dense_attn_fwd.restype = _i
+            L.linformer_pool_peak_bytes.argtypes = [_i]
+            L.linformer_pool_peak_bytes.restype = ctypes.c_int64
             L.linformer_attn_bwd.argtypes = [_vp] * 12 + [_i] * 7 + [_vp]
             L.linformer_attn_bwd.restype = _i
             L.linformer_window_projection.argtypes = [_vp, _vp, _i, _i, _i, _vp]
@@ -263,3 +268,24 @@ def attention_backward(Q, K, V, E, F, lengths, dO, share_mode: int = PER_HEAD, s
     if st != 0:
         raise LinformerError(st, "linformer_attn_bwd")
     return dQ, dK, dV, dE, dF
+
+
+def linformer_dense_attn_fwd(Q, K, V, pad_lengths, O, b, h, n, d, dtype, stream=None) -> int:
+    return lib().linformer_dense_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(pad_lengths), _ptr(O),
+                                          b, h, n, d, dtype, _stream_handle(stream))
+
+
+def linformer_pool_peak_bytes(reset: bool = False) -> int:
+    return lib().linformer_pool_peak_bytes(1 if reset else 0)
+
+
+def dense_attention(Q, K, V, lengths=None, out=None, stream=None):
+    """O = softmax(Q K^T / sqrt(d)) V of device fp32 tensors [b][h][n][d] (allocates O)."""
+    import torch
+    b, h, n, d = Q.shape
+    if out is None:
+        out = torch.empty((b, h, n, d), dtype=torch.float32, device=Q.device)
+    st = linformer_dense_attn_fwd(Q, K, V, lengths, out, b, h, n, d, dtype_code(Q), stream)
+    if st != 0:
+        raise LinformerError(st, "linformer_dense_attn_fwd")
+    return out

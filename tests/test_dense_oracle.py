@@ -86,3 +86,12 @@ def test_pins_catch_planted_mistakes(bad, monkeypatch):
     monkeypatch.setattr(dense, "dense_fwd", wrong)
     with pytest.raises(AssertionError):
         test_equals_linformer_with_identity_projections()
+
+
+def test_row_subsets_match_the_whole():
+    rng = np.random.default_rng(4)
+    Q, K, V = (rng.standard_normal((2, 2, 30, 8)) for _ in range(3))
+    lengths = np.array([17, 30])
+    full = dense.dense_fwd(Q, K, V, lengths)
+    rows = np.array([0, 16, 17, 29])
+    assert np.array_equal(dense.dense_fwd(Q, K, V, lengths, rows=rows), full[:, :, rows])

@@ -465,7 +465,7 @@ def run_backward(args):
     libbuild.build()
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    c = BWD_SHAPE
+    c = dict(BWD_SHAPE, b=args.batch) if args.batch else BWD_SHAPE
     b, h, n, d, k, mode = c["b"], c["h"], c["n"], c["d"], c["k"], c["share_mode"]
     x = make_inputs(b, h, n, d, k, mode, 0, seed=77)
     dO_h = output_gradient(b, h, n, d, seed=78)
@@ -517,8 +517,8 @@ def run_backward(args):
         "value": tokens / (ms_step * 1e-3) / 1e6, "unit": UNIT, "n_gpus": 1, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "bwd_b16_h12_n4096_d64_k256_layerwise", **c,
-                   "l2": "inputs larger than L2 (805 MB of Q, K, V, dO)"},
+        "config": {"workload": f"bwd_b{b}_h12_n4096_d64_k256_layerwise", **c,
+                   "l2": f"inputs of {4 * b * h * n * d * 4 / 1e6:.0f} MB (Q, K, V, dO)"},
         "roofline": {"kernel": "backward (all launches)", "bound": "alu",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,

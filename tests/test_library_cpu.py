@@ -121,3 +121,22 @@ def test_backward_argument_errors_are_reported_before_launch(L, args, expected):
                                a["dQ"], a["dK"], a["dV"], a["dE"], a["dF"], a["b"], a["h"],
                                a["n"], a["d"], a["k"], a["share_mode"], a["dtype"], stream=0)
     assert st == expected, lf.status_string(st)
+
+
+@pytest.mark.parametrize("args,expected", [
+    (dict(O=None), -1),
+    (dict(V=None), -1),
+    (dict(dtype=1), -3),                        # fp32 only
+    (dict(d=129), -3),
+    (dict(n=0), -2),
+    (dict(b=300, h=300), -2),                   # more than 65535 units
+    (dict(K=A + 4), -5),
+    (dict(pad=A + 2), -5),
+    (dict(dtype=9), -4),
+])
+def test_dense_argument_errors_are_reported_before_launch(L, args, expected):
+    a = dict(Q=A, K=A, V=A, pad=None, O=A, b=2, h=3, n=64, d=64, dtype=0)
+    a.update(args)
+    st = lf.linformer_dense_attn_fwd(a["Q"], a["K"], a["V"], a["pad"], a["O"], a["b"], a["h"],
+                                     a["n"], a["d"], a["dtype"], stream=0)
+    assert st == expected, lf.status_string(st)

@@ -53,10 +53,11 @@ int *device_status_ptr();
 int workspace_alloc(void **ptr, size_t bytes, cudaStream_t s);
 void workspace_free(void *ptr, cudaStream_t s);
 
-// Process-wide P.Vbar product-count setting (0 = automatic, 1 or 3).
+// Process-wide P.Vbar product-count setting (0 = automatic, 1, 2 or 3).
 int pv_terms_setting();
 
-// fp32 SIMT kernels (simt_kernels.cu).
+// Fused SIMT kernels for bf16 inputs off the tensor-core shapes (simt_kernels.cu);
+// fp32 inputs return LINFORMER_ERR_UNSUPPORTED (they run on simt_gemm.cu).
 int simt_project(const Problem &p, float *Kbar, float *Vbar);
 int simt_attend(const Problem &p, const float *Kbar, const float *Vbar);
 

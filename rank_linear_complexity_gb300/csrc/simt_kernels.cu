@@ -1,9 +1,8 @@
-// fp32 FFMA kernels for the Linformer attention forward.
-//
-// They serve the fp32 dtype (whose tolerance rules out reduced-precision tensor
-// cores) and every shape outside the tensor-core path (d != 64, k > 256, n not
-// a multiple of 8).  All arithmetic is fp32; the projection accumulates over the
-// sequence in order, the softmax is the exact two-pass form.
+// Fused FFMA kernels for the Linformer attention forward on bf16 inputs whose shape
+// is outside the tensor-core path (d != 64, k > 256, n not a multiple of 8).  fp32
+// inputs run on the matrix-product kernels of simt_gemm.cu instead.  All arithmetic
+// is fp32; the projection accumulates over the sequence in order, the softmax is the
+// exact two-pass form.
 //
 // Steps ("Linformer(Self-Attention with Linear Complexity) 요약 설명", section Model):
 //   simt_project_kernel: Kbar = Ehat . K and Vbar = Fhat . V over rows t < L.
@@ -16,7 +15,6 @@
 namespace linformer {
 namespace {
 
-__device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
@@ -153,22 +151,17 @@ __global__ void __launch_bounds__(AW * 32) simt_attend_kernel(
 
 int simt_project(const Problem &p, float *Kbar, float *Vbar) {
     dim3 grid((unsigned)p.units(), (unsigned)((p.k + PJ - 1) / PJ), 2);
+    if (p.dtype == LINFORMER_F32) return LINFORMER_ERR_UNSUPPORTED;  // simt_gemm.cu's
     KernelScope scope(LINFORMER_KERNEL_PROJECT_SIMT, p.stream);
-    if (p.dtype == LINFORMER_F32) {
-        simt_project_kernel<float><<<grid, 256, 0, p.stream>>>(
-            (const float *)p.K, (const float *)p.V, (const float *)p.E,
-            (const float *)p.f_or_e(), p.pad, Kbar, Vbar, p.h, p.n, p.d, p.k,
-            p.proj_per_head() ? 1 : 0);
-    } else {
-        simt_project_kernel<__nv_bfloat16><<<grid, 256, 0, p.stream>>>(
-            (const __nv_bfloat16 *)p.K, (const __nv_bfloat16 *)p.V,
-            (const __nv_bfloat16 *)p.E, (const __nv_bfloat16 *)p.f_or_e(), p.pad, Kbar, Vbar,
-            p.h, p.n, p.d, p.k, p.proj_per_head() ? 1 : 0);
-    }
+    simt_project_kernel<__nv_bfloat16><<<grid, 256, 0, p.stream>>>(
+        (const __nv_bfloat16 *)p.K, (const __nv_bfloat16 *)p.V, (const __nv_bfloat16 *)p.E,
+        (const __nv_bfloat16 *)p.f_or_e(), p.pad, Kbar, Vbar, p.h, p.n, p.d, p.k,
+        p.proj_per_head() ? 1 : 0);
     return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
 }
 
 int simt_attend(const Problem &p, const float *Kbar, const float *Vbar) {
+    if (p.dtype == LINFORMER_F32) return LINFORMER_ERR_UNSUPPORTED;  // simt_gemm.cu's
     const int64_t tiles = (p.n + AROWS - 1) / AROWS;
     const int64_t blocks = p.units() * tiles;
     if (blocks > 0x7fffffffLL) return LINFORMER_ERR_SIZE;
@@ -184,9 +177,7 @@ int simt_attend(const Problem &p, const float *Kbar, const float *Vbar) {
             kern<<<(unsigned)blocks, AW * 32, smem, p.stream>>>(                           \
                 (const TI *)p.Q, Kbar, Vbar, p.pad, (TO *)p.O, p.h, p.n, p.d, p.k, tiles); \
     } while (0)
-    if (p.dtype == LINFORMER_F32)
-        LAUNCH_ATTEND(float, float);
-    else if (p.dtype == LINFORMER_BF16)
+    if (p.dtype == LINFORMER_BF16)
         LAUNCH_ATTEND(__nv_bfloat16, __nv_bfloat16);
     else
         LAUNCH_ATTEND(__nv_bfloat16, float);

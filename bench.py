@@ -569,7 +569,11 @@ def run_inference_table(args):
     h, d = TABLE_H, TABLE_D
     rows = []
 
-    def measure(fn, seqs, io_bytes_per_seq, fixed_bytes, steps):
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    f32_peak = sms * 128 * 2 * 2070e6 / 1e12  # fp32 FMA lanes x 2 FLOPs x max clock
+    bf16_peak = load_peaks()["bf16_tflops"]
+
+    def measure(fn, seqs, io_bytes_per_seq, fixed_bytes, steps, flop_per_seq, peak):
         torch.cuda.synchronize()
         lf.linformer_pool_peak_bytes(reset=True)
         fn()
@@ -577,7 +581,9 @@ def run_inference_table(args):
         ws = lf.linformer_pool_peak_bytes()
         ms = time_call(fn, steps, 2, stream)
         per_seq = io_bytes_per_seq + ws / seqs
+        tflops = flop_per_seq / (ms / seqs * 1e-3) / 1e12
         return {"ms_per_seq": ms / seqs, "bytes_per_seq": per_seq,
+                "tflops": tflops, "frac_of_peak": tflops / peak,
                 "max_batch_16GB": int(max(0, V100_BYTES - fixed_bytes) // per_seq),
                 "max_batch_hbm": int(max(0, hbm - fixed_bytes) // per_seq)}
 
@@ -590,7 +596,8 @@ def run_inference_table(args):
         O = torch.empty_like(Q)
         seqs = bd * hd / h
         fn = lambda: lf.dense_attention(Q, K, V, out=O)
-        row["dense_f32"] = measure(fn, seqs, 4 * h * n * d * 4, 0, 3 if n > 4096 else 10)
+        row["dense_f32"] = measure(fn, seqs, 4 * h * n * d * 4, 0, 3 if n > 4096 else 10,
+                                   4.0 * h * n * n * d, f32_peak)
         del Q, K, V, O, x
         # Linformer, one E = F shared by all heads (layerwise), fp32 and bf16 inputs
         bl = 16 if n <= 4096 else 1
@@ -600,7 +607,8 @@ def run_inference_table(args):
             O = torch.empty_like(g["Q"])
             es = 4 if dt == 0 else 2
             fn = lambda: lf.attention(g["Q"], g["K"], g["V"], g["E"], None, None, 3, out=O)
-            row[name] = measure(fn, bl, 4 * h * n * d * es, k * n * es, 10)
+            row[name] = measure(fn, bl, 4 * h * n * d * es, k * n * es, 10, 8.0 * h * n * k * d,
+                                f32_peak if dt == 0 else bf16_peak)
             del g, O, x
         for name in ("linformer_f32", "linformer_bf16"):
             row[name]["speedup_vs_dense_f32"] = (row["dense_f32"]["ms_per_seq"] /
@@ -614,7 +622,10 @@ def run_inference_table(args):
     print(json.dumps({"experiment": "inference_table", "h": h, "d": d,
                       "share_mode": "layerwise (one E = F)", "hbm_bytes": hbm,
                       "note": "attention only, one layer; dense keeps the n x n scores of "
-                              "every head in device memory; ms per sequence of 12 heads",
+                              "every head in device memory; ms per sequence of 12 heads; "
+                              "algorithmic FLOPs 4 n^2 d (dense), 8 n k d (Linformer) per "
+                              "head; peaks: fp32 derived from SMs x 128 lanes x 2 x 2070 MHz "
+                              "(f32 rows), measured bf16 (bf16 rows)",
                       "rows": rows}))
     return 0
 

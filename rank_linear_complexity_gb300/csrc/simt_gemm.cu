@@ -16,107 +16,97 @@ __device__ __forceinline__ int unit_length(const int32_t *pad, int unit, int h, 
     return L < 0 ? 0 : (L > n ? n : L);
 }
 
-// Register staging of one BX x kBK operand tile: BX / 16 elements per thread, taken as
-// groups of four along the contiguous axis (a group is wholly in or out of range
-// when vec is set: the contiguous extent is then a multiple of four).
+constexpr int kStages = 3;  // shared-memory slabs in flight
+
+__device__ __forceinline__ void cp_async16(float *dst, const float *src, int src_bytes) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(float *dst, const float *src, int src_bytes) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(d), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Asynchronous copy of one BX x kBK operand tile (x0.., k0..) into s[kk][x] (row stride
+// BX + 4).  Elements out of range or masked are zero-filled by the copy itself (a
+// source size of 0, or fewer than 16 bytes at the edge of a masked range); their
+// source address is then the matrix base, which is never read.  Groups of four along
+// a contiguous x go as 16-byte copies (vec); everything else, the transposing kk-fast
+// case included, as 4-byte copies laid out so that a warp reads whole 64-byte rows.
 template <int BX>
-struct Stage {
-    static constexpr int kGroups = BX / 64;  // groups of four per thread
-    float v[kGroups][4];
-
-    __device__ __forceinline__ void load(const Operand &o, const float *m, int x0, int k0, int X,
-                                         int K, int L) {
+__device__ __forceinline__ void copy_tile(const Operand &o, const float *m, int x0, int k0, int X,
+                                          int K, int L, float *s) {
+    if (o.xfast && o.vec) {
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
+        for (int g = 0; g < BX / 64; ++g) {
             const int idx = threadIdx.x + g * kThreads;
-            int x, kk;
-            if (o.xfast) {
-                x = x0 + (idx % (BX / 4)) * 4;
-                kk = k0 + idx / (BX / 4);
-            } else {
-                x = x0 + idx / (kBK / 4);
-                kk = k0 + (idx % (kBK / 4)) * 4;
+            const int xr = (idx % (BX / 4)) * 4, kk = idx / (BX / 4);
+            const int x = x0 + xr, ka = k0 + kk;
+            int bytes = 0;
+            if (x < X && ka < K && !(o.mask_k && ka >= L)) {
+                const int lim = o.mask_x ? min(4, L - x) : 4;
+                bytes = lim > 0 ? lim * 4 : 0;
             }
-            if (o.vec) {
-                const bool in = x < X && kk < K;
-                float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (in) {
-                    const long long off = o.xfast ? (long long)kk * o.ld + x : (long long)x * o.ld + kk;
-                    q = __ldg(reinterpret_cast<const float4 *>(m + off));
-                }
-                v[g][0] = q.x;
-                v[g][1] = q.y;
-                v[g][2] = q.z;
-                v[g][3] = q.w;
-            } else {
+            cp_async16(s + kk * (BX + 4) + xr, bytes ? m + (long long)ka * o.ld + x : m, bytes);
+        }
+    } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int xe = o.xfast ? x + e : x, ke = o.xfast ? kk : kk + e;
-                    v[g][e] = (xe < X && ke < K)
-                                  ? __ldg(m + (o.xfast ? (long long)ke * o.ld + xe
-                                                       : (long long)xe * o.ld + ke))
-                                  : 0.f;
-                }
-            }
-            if (o.mask_x | o.mask_k) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int xe = o.xfast ? x + e : x, ke = o.xfast ? kk : kk + e;
-                    if ((o.mask_x && xe >= L) || (o.mask_k && ke >= L)) v[g][e] = 0.f;
-                }
-            }
+        for (int e = 0; e < BX / 16; ++e) {
+            const int idx = threadIdx.x + e * kThreads;
+            const int xr = o.xfast ? idx % BX : idx / kBK;
+            const int kk = o.xfast ? idx / BX : idx % kBK;
+            const int x = x0 + xr, ka = k0 + kk;
+            const bool in = x < X && ka < K && !(o.mask_x && x >= L) && !(o.mask_k && ka >= L);
+            const long long off = o.xfast ? (long long)ka * o.ld + x : (long long)x * o.ld + ka;
+            cp_async4(s + kk * (BX + 4) + xr, in ? m + off : m, in ? 4 : 0);
         }
     }
-
-    // into s[kk][x] (row stride BX + 4)
-    __device__ __forceinline__ void store(const Operand &o, float *s) const {
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-            const int idx = threadIdx.x + g * kThreads;
-            if (o.xfast) {
-                const int x = (idx % (BX / 4)) * 4, kk = idx / (BX / 4);
-                *reinterpret_cast<float4 *>(s + kk * (BX + 4) + x) =
-                    make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
-            } else {
-                const int x = idx / (kBK / 4), kk = (idx % (kBK / 4)) * 4;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) s[(kk + e) * (BX + 4) + x] = v[g][e];
-            }
-        }
-    }
-};
+}
 
 // One BM x BN output tile of unit blockIdx.z per CTA.  Thread (tx, ty) owns rows
 // ty*4 + {0..3} (+ 64, + 128 ... for BM > 64) and columns tx*4 + {0..3} (+ 64 ...), so
-// its shared-memory reads are 16-byte loads that a warp serves in two passes.  The
-// next tile's global loads are in registers while the current one is multiplied.
+// its shared-memory reads are 16-byte loads that a warp serves in two passes.  Slabs
+// of kBK arrive by asynchronous copies kStages - 1 steps ahead of their use; one
+// barrier per step both publishes the arrived slab and frees the one about to be
+// overwritten.  Dynamic shared memory: kStages * kBK * (BM + BN + 8) floats.
 template <int BM, int BN>
 __global__ void __launch_bounds__(kThreads, 2) batched_gemm_kernel(const GemmArgs g) {
     constexpr int TM = BM / 16, TN = BN / 16;
-    __shared__ __align__(16) float sA[2][kBK * (BM + 4)];
-    __shared__ __align__(16) float sB[2][kBK * (BN + 4)];
+    constexpr int SA = kBK * (BM + 4), SB = kBK * (BN + 4);
+    extern __shared__ __align__(16) float smem[];
+    float *sA = smem, *sB = smem + kStages * SA;
     const int z = blockIdx.z, tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int tiles_n = gridDim.x / g.splits, split = blockIdx.x / tiles_n;
     const int row0 = blockIdx.y * BM, col0 = (blockIdx.x % tiles_n) * BN;
     const int kbeg = split * g.kchunk, kend = min(g.K, kbeg + g.kchunk);
+    const int nslabs = kend > kbeg ? (kend - kbeg + kBK - 1) / kBK : 0;
     const float *A = g.A.mat(z, g.h), *B = g.B.mat(z, g.h);
     const int L = unit_length(g.pad, z, g.h, g.n);
-    Stage<BM> ra;
-    Stage<BN> rb;
     float acc[TM][TN] = {};
-    ra.load(g.A, A, row0, kbeg, g.M, kend, L);
-    rb.load(g.B, B, col0, kbeg, g.N, kend, L);
-    ra.store(g.A, sA[0]);
-    rb.store(g.B, sB[0]);
-    __syncthreads();
-    int buf = 0;
-    for (int k0 = kbeg; k0 < kend; k0 += kBK) {
-        const bool more = k0 + kBK < kend;
-        if (more) {
-            ra.load(g.A, A, row0, k0 + kBK, g.M, kend, L);
-            rb.load(g.B, B, col0, k0 + kBK, g.N, kend, L);
+    auto issue = [&](int slab) {
+        if (slab < nslabs) {
+            const int k0 = kbeg + slab * kBK, st = slab % kStages;
+            copy_tile<BM>(g.A, A, row0, k0, g.M, kend, L, sA + st * SA);
+            copy_tile<BN>(g.B, B, col0, k0, g.N, kend, L, sB + st * SB);
         }
-        const float *a_s = sA[buf], *b_s = sB[buf];
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int st = 0; st < kStages - 1; ++st) issue(st);
+    for (int it = 0; it < nslabs; ++it) {
+        cp_async_wait<kStages - 2>();
+        __syncthreads();
+        issue(it + kStages - 1);
+        const float *a_s = sA + (it % kStages) * SA, *b_s = sB + (it % kStages) * SB;
 #pragma unroll
         for (int kk = 0; kk < kBK; ++kk) {
             float a[TM], b[TN];
@@ -141,13 +131,8 @@ __global__ void __launch_bounds__(kThreads, 2) batched_gemm_kernel(const GemmArg
 #pragma unroll
                 for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
-        if (more) {
-            buf ^= 1;
-            ra.store(g.A, sA[buf]);
-            rb.store(g.B, sB[buf]);
-        }
-        __syncthreads();
     }
+    cp_async_wait<0>();
     if (g.splits > 1) {
         float *Pt = g.part + ((long long)split * gridDim.z + z) * g.M * g.N;
 #pragma unroll
@@ -246,9 +231,13 @@ int launch_gemm(const GemmArgs &g, int units, cudaStream_t s, int kernel_id) {
     const long long gx = (long long)((g.N + BN - 1) / BN) * g.splits;
     dim3 grid((unsigned)gx, (unsigned)((g.M + BM - 1) / BM), (unsigned)units);
     if (gx > 0x7fffffffLL || grid.y > 65535u || grid.z > 65535u) return LINFORMER_ERR_SIZE;
+    constexpr size_t smem = sizeof(float) * kStages * kBK * (BM + BN + 8);
+    if (cudaFuncSetAttribute(batched_gemm_kernel<BM, BN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LINFORMER_ERR_LAUNCH;
     {
         KernelScope scope(kernel_id, s);
-        batched_gemm_kernel<BM, BN><<<grid, kThreads, 0, s>>>(g);
+        batched_gemm_kernel<BM, BN><<<grid, kThreads, smem, s>>>(g);
     }
     if (g.splits > 1) {
         const long long total = (long long)units * g.M * g.N;

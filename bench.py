@@ -533,8 +533,9 @@ def run_backward(args):
     return 0
 
 
-# The pages' single-GPU inference table: (n, k) pairs, RoBERTa-base heads (h = 12, d = 64).
-TABLE_POINTS = [(512, 128), (4096, 128), (4096, 256), (65536, 128), (65536, 256)]
+# The pages' single-GPU inference table: n in {512, 4096, 65536}, k in {128, 256},
+# RoBERTa-base heads (h = 12, d = 64).
+TABLE_POINTS = [(512, 128), (512, 256), (4096, 128), (4096, 256), (65536, 128), (65536, 256)]
 TABLE_H, TABLE_D = 12, 64
 V100_BYTES = 16e9  # the pages' GPU capacity
 

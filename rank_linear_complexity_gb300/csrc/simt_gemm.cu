@@ -40,8 +40,9 @@ __device__ __forceinline__ void cp_async_wait() {
 // BX + 4).  Elements out of range or masked are zero-filled by the copy itself (a
 // source size of 0, or fewer than 16 bytes at the edge of a masked range); their
 // source address is then the matrix base, which is never read.  Groups of four along
-// a contiguous x go as 16-byte copies (vec); everything else, the transposing kk-fast
-// case included, as 4-byte copies laid out so that a warp reads whole 64-byte rows.
+// a contiguous x go as 16-byte copies (vec); everything else as 4-byte copies in
+// which consecutive threads read consecutive addresses (in the transposing kk-fast
+// case, 16 threads read one 64-byte row segment).
 template <int BX>
 __device__ __forceinline__ void copy_tile(const Operand &o, const float *m, int x0, int k0, int X,
                                           int K, int L, float *s) {

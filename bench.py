@@ -83,6 +83,38 @@ def algorithmic(w):
     }
 
 
+def valid_rows_algorithmic(w, lengths):
+    """Compulsory bytes and FLOPs over the valid rows only (ragged batches): Q, K, V and
+    the FLOPs of rows t < L_b, all of O (padded rows are written as zero), E and F once."""
+    es = 4 if w.dtype == 0 else 2
+    os_ = 2 if w.dtype == 1 else 4
+    rows = sum(min(max(int(L), 0), w.n) for L in lengths) * w.h
+    groups = w.h if w.share_mode in (0, 1) else 1
+    n_proj = 2 if w.share_mode in (0, 2) else 1
+    return {"total_bytes": 3 * rows * w.d * es + w.units * w.n * w.d * os_
+                           + groups * n_proj * w.k * w.n * es,
+            "total_flop": 8.0 * rows * w.k * w.d}
+
+
+def flushed_median(step, stream, steps: int, scratch_bytes: int = 1 << 30):
+    """Per-step device time with L2 flushed before every step (a 1 GB write between the
+    steps, outside the events): median and spread over `steps` steps, in ms."""
+    scratch = torch.empty(scratch_bytes, dtype=torch.uint8, device=stream.device)
+    pairs = []
+    for i in range(steps):
+        scratch.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in pairs)
+    del scratch
+    return {"median_ms": statistics.median(ms), "min_ms": ms[0], "max_ms": ms[-1],
+            "steps": steps, "flush": f"{scratch_bytes >> 20} MB write before each step"}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason sampling while the GPU works."""
 
@@ -322,6 +354,22 @@ def run_ours(args):
     t_roof = max(alg["total_bytes"] / (peaks["hbm_gbs"] * 1e9),
                  alg["total_flop"] / (peaks["bf16_tflops"] * 1e12))
     path_frac = t_roof / (ms_step * 1e-3)
+    valid_frac = None
+    if x["lengths"] is not None:
+        va = valid_rows_algorithmic(w, x["lengths"].tolist())
+        valid_frac = max(va["total_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                         va["total_flop"] / (peaks["bf16_tflops"] * 1e12)) / (ms_step * 1e-3)
+
+    # --- L2 flushed before every step: median of up to 50 single-step timings ---------
+    flushed = None
+    if not args.no_flush_pass:
+        try:
+            flushed = flushed_median(step, stream, max(1, min(args.steps, 50)))
+            flushed["value"] = aggregate_throughput(w.tokens, flushed["median_ms"], world)
+        except (RuntimeError, torch.cuda.OutOfMemoryError) as e:  # no room for the scratch
+            flushed = {"unavailable": str(e).splitlines()[0][:200]}
+        if lf.linformer_debug_read_device_status(stream) != 0:
+            raise RuntimeError("device status set during the flushed pass")
 
     # --- end to end through the host-buffer entry point -------------------------------
     e2e = None
@@ -369,6 +417,8 @@ def run_ours(args):
                                f"{L2_BYTES / 1e6:.0f} MB L2)")),
             "tflops": alg["total_flop"] / (ms_step * 1e-3) / 1e12,
             "path_roofline_frac": path_frac,
+            "path_roofline_frac_valid_rows": valid_frac,
+            "l2_flushed": flushed,
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks,
         }
@@ -648,6 +698,8 @@ def main():
                     help="--impl reference: seconds for all warm-up + timed steps")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush-pass", action="store_true",
+                    help="skip the extra pass timed with L2 flushed before every step")
     ap.add_argument("--approx-error", action="store_true",
                     help="report the method's approximation error over n and k instead")
     ap.add_argument("--backward", action="store_true",

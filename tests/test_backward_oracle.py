@@ -62,21 +62,59 @@ def forward_torch(Q, K, V, E, F, lengths, mode):
     return torch.stack(out)
 
 
-@pytest.mark.parametrize("mode", [PER_HEAD, KV, HEADWISE, LAYERWISE])
-def test_autograd(mode):
+def check_autograd(mode, oracle_bwd=None):
+    oracle_bwd = oracle_bwd or bw.linformer_bwd
     b, h, n, d, k = 2, 3, 40, 16, 12
     x = case_inputs(b, h, n, d, k, mode, F32, ragged=True, seed=20 + mode)
     t = {kk: (v.double().requires_grad_(True) if v is not None and v.dtype.is_floating_point else v)
          for kk, v in x.items()}
     W = torch.randn(b, h, n, d, dtype=torch.float64, generator=torch.Generator().manual_seed(mode))
     (forward_torch(t["Q"], t["K"], t["V"], t["E"], t["F"], x["lengths"], mode) * W).sum().backward()
-    dQ, dK, dV, dE, dF = bw.linformer_bwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
-                                          W.numpy(), mode)
+    dQ, dK, dV, dE, dF = oracle_bwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                    W.numpy(), mode)
     pairs = [(dQ, t["Q"]), (dK, t["K"]), (dV, t["V"]), (dE, t["E"])]
     if dF is not None:
         pairs.append((dF, t["F"]))
     for got, ref in pairs:
         assert np.abs(got - ref.grad.numpy()).max() <= 1e-10 * max(1.0, ref.grad.abs().max().item())
+
+
+@pytest.mark.parametrize("mode", [PER_HEAD, KV, HEADWISE, LAYERWISE])
+def test_autograd(mode):
+    check_autograd(mode)
+
+
+# Plausible mistakes, each planted in a copy of the oracle's source: every one must make
+# the autograd pin fail in at least one sharing mode.  (Keeping dO's padded rows is not
+# among them: P's padded rows are zero, so those rows reach no gradient.)
+PLANTED = {
+    "dQ without the 1/sqrt(d) scale": ("dQ[bi, hi] = (dS @ Kb) * scale", "dQ[bi, hi] = dS @ Kb"),
+    "softmax backward without the row-sum term": (
+        "dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))", "dS = P * dP"),
+    "dVbar scaled by 1/sqrt(d) as well": ("dVb = P.T @ G", "dVb = (P.T @ G) * scale"),
+    "padded dK rows not zeroed": ("dK[bi, hi, L:] = 0.0", "pass"),
+    "F term dropped when F is E": ("(dE[hi] if per_head else dE)[...] += gE + gF",
+                                   "(dE[hi] if per_head else dE)[...] += gE"),
+    "shared E overwritten instead of summed": (
+        "(dE[hi] if per_head else dE)[...] += gE\n", "(dE[hi] if per_head else dE)[...] = gE\n"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PLANTED))
+def test_planted_mistakes_are_caught(name):
+    import types
+    old, new = PLANTED[name]
+    src = open(bw.__file__).read()
+    assert src.count(old) == 1, f"planting site not found: {old}"
+    mod = types.ModuleType("planted_backward")
+    exec(compile(src.replace(old, new), "planted_backward", "exec"), mod.__dict__)
+    caught = 0
+    for mode in (PER_HEAD, KV, HEADWISE, LAYERWISE):
+        try:
+            check_autograd(mode, mod.linformer_bwd)
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no pin fails with the mistake: {name}"
 
 
 def test_identity_projection_is_attention_backward():

@@ -248,6 +248,14 @@ LINFORMER_API const char *linformer_status_string(int status);
  * clears it), else LINFORMER_OK.  For tests and debugging. */
 LINFORMER_API int linformer_debug_read_device_status(void *stream);
 
+/* Test of the device-side failure path: launches one warp on `stream` that waits,
+ * through the same bounded wait as the kernels, on a barrier nothing completes.  After
+ * the wait limit (2 s) the warp records a failure in the device status word and exits;
+ * no fault, trap or hang.  Returns LINFORMER_OK once launched;
+ * linformer_debug_read_device_status() then reports LINFORMER_ERR_DEVICE, and the
+ * library keeps working on the same context.  For tests and debugging. */
+LINFORMER_API int linformer_debug_wait_probe(void *stream);
+
 /* Number of products in the P.Vbar step of the tensor-core path: 0 = chosen per
  * unit on the device from max|Vbar| (default: 1 below 24, 2 below 40, else 3),
  * 1 = one product (fp16 P, fp16 Vbar), 2 = P times the hi/lo split of Vbar,

@@ -31,7 +31,7 @@ SYMBOLS = [
     "linformer_set_pv_terms", "linformer_launch_count", "linformer_profile_enable",
     "linformer_profile_collect", "linformer_kernel_name", "linformer_attn_fwd_noalloc",
     "linformer_window_projection", "linformer_attn_bwd", "linformer_dense_attn_fwd",
-    "linformer_pool_peak_bytes",
+    "linformer_pool_peak_bytes", "linformer_debug_wait_probe",
 ]
 
 
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
             L.linformer_profile_collect.restype = _i
             L.linformer_dense_attn_fwd.argtypes = [_vp] * 5 + [_i] * 5 + [_vp]
             L.linformer_dense_attn_fwd.restype = _i
+            L.linformer_debug_wait_probe.argtypes = [_vp]
+            L.linformer_debug_wait_probe.restype = _i
             L.linformer_pool_peak_bytes.argtypes = [_i]
             L.linformer_pool_peak_bytes.restype = ctypes.c_int64
             L.linformer_attn_bwd.argtypes = [_vp] * 12 + [_i] * 7 + [_vp]
@@ -154,6 +156,10 @@ def status_string(status: int) -> str:
 
 def linformer_debug_read_device_status(stream=None) -> int:
     return lib().linformer_debug_read_device_status(_stream_handle(stream))
+
+
+def linformer_debug_wait_probe(stream=None) -> int:
+    return lib().linformer_debug_wait_probe(_stream_handle(stream))
 
 
 def linformer_set_pv_terms(terms: int) -> int:

@@ -26,3 +26,28 @@ def test_valid_rows_scale_with_the_valid_rows_only():
     assert full["total_bytes"] - half["total_bytes"] == 3 * units_rows * w.d * es
     clamped = bench.valid_rows_algorithmic(w, [w.n + 5, -3])
     assert clamped == half
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON line
+    with the fields the measurement contract asks for; a tiny time budget here."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "3", "--ref-budget-s", "3"],
+                         capture_output=True, text=True, timeout=600, cwd=root,
+                         env=dict(os.environ, RANK="0", WORLD_SIZE="1"))
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["unit"] == "Mtokens/s" and j["value"] > 0
+    assert j["steps"] == 2 and j["warmup"] == 3 and j["higher_is_better"] is True
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["cpu_baseline"]["value"] == j["value"]
+    assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert j["config"]["workload"] == "bf16_b16h12_n4096_k256_layerwise"

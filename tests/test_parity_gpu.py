@@ -2,8 +2,8 @@
 
 Small cases are compared element by element over the whole output; the five
 evaluation workloads run at full size in the same call the benchmark times and
-are compared on sampled units and rows (the oracle computes those one by one),
-plus properties that hold at any size (finite values, zero padded rows).
+are compared element by element with the whole-problem oracle as well (it runs
+on all host cores in seconds), plus exact zeros on the padded rows.
 """
 import numpy as np
 import pytest
@@ -224,29 +224,33 @@ def test_pv_products_match_oracle(terms, vscale):
     check(host64(O), ref, BF16, f"terms={terms} vscale={vscale}")
 
 
-# --- the five evaluation workloads at full size, sampled ------------------------------
+# --- the five evaluation workloads at full size, whole output ------------------------
 
-def sample_rows(n, L, rng, count=192):
-    picks = {0, n - 1, max(0, L - 1), min(n - 1, L), 127, 128, min(n - 1, 129)}
-    picks.update(rng.integers(0, n, size=count).tolist())
-    return np.array(sorted(p for p in picks if 0 <= p < n), np.int64)
+def _report(entry):
+    """Appends one JSON line of parity margins to $LINFORMER_PARITY_REPORT, if set."""
+    import json
+    import os
+    path = os.environ.get("LINFORMER_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(entry) + "\n")
+    print(entry)
 
 
 @pytest.mark.parametrize("wi", range(len(WORKLOADS)), ids=[w.name for w in WORKLOADS])
-def test_workload_full_size_sampled(wi):
+def test_workload_full_output(wi):
+    """Every element of the five evaluation workloads, in the launch configuration the
+    benchmark times, against the whole-problem fp64 oracle on all host cores."""
     w = WORKLOADS[wi]
     x = workload_inputs(w)
     O = run(x, w.share_mode, w.dtype)
-    assert torch.isfinite(O.float()).all()
-    rng = np.random.default_rng(wi)
     lengths = x["lengths"].numpy() if x["lengths"] is not None else np.full(w.b, w.n)
     for bi in range(w.b):
         assert (O[bi, :, int(lengths[bi]):] == 0).all()
-    units = {(0, 0), (w.b - 1, w.h - 1)}
-    units.update((int(rng.integers(w.b)), int(rng.integers(w.h))) for _ in range(2))
-    for (bi, hi) in sorted(units):
-        rows = sample_rows(w.n, int(lengths[bi]), rng)
-        ref, _, _ = orc.unit_rows(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
-                                  w.share_mode, bi, hi, rows)
-        got = host64(O[bi, hi][torch.from_numpy(rows).to(DEV)])
-        check(got, ref, w.dtype, f"{w.name} unit ({bi},{hi})")
+    got = host64(O)
+    del O
+    ref, used = orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                  w.share_mode)
+    e = check(got, ref, w.dtype, w.name)
+    _report({"workload": w.name, "elements": int(ref.size), "oracle_threads": int(used),
+             **{kk: (round(v, 6) if isinstance(v, float) else v) for kk, v in e.items()}})

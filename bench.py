@@ -116,52 +116,100 @@ def flushed_median(step, stream, steps: int, scratch_bytes: int = 1 << 30):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling while the GPU works."""
+    """nvidia-smi clock / throttle-reason sampling while the GPU works.  Each sample is
+    stamped with the host clock when it arrives, so that windows of the run (the timed
+    steps, the sustained pass) can be summarised separately."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 50):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
+        self.thread = None
+        self.samples = []  # (host monotonic time, row)
 
     def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                row = next(csv.reader([line]), [])
+                if len(row) >= 9:
+                    self.samples.append((time.monotonic(), row))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def wait_first(self, timeout_s: float = 5.0):
+        """Blocks until the first sample has arrived (nvidia-smi takes a moment to start)."""
+        t0 = time.monotonic()
+        while self.proc is not None and not self.samples and time.monotonic() - t0 < timeout_s:
+            time.sleep(0.01)
 
     def stop(self):
+        if self.proc is not None:
+            self.proc.send_signal(signal.SIGTERM)
+            try:
+                self.proc.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=10)
+
+    def summary(self, t0: float = None, t1: float = None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
                     "samples": 0}
-        self.proc.send_signal(signal.SIGTERM)
-        try:
-            out, _ = self.proc.communicate(timeout=10)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
         sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for t, r in self.samples:
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             try:
                 sm.append(float(r[1]))
                 smax.append(float(r[2]))
                 power.append(float(r[3]))
             except ValueError:
                 continue
-            for name, val in zip(names, r[5:9]):
+            for name, val in zip(self.REASONS, r[5:9]):
                 if val.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def sustained_pass(step, stream, seconds: float, batch: int = 100):
+    """Back-to-back steps for at least `seconds` (batches of `batch` steps, synchronised
+    after each), timed with CUDA events; returns (ms per step, steps, host t0, host t1)."""
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.monotonic()
+    ev0.record(stream)
+    steps = 0
+    while True:
+        for _ in range(batch):
+            step()
+        steps += batch
+        torch.cuda.synchronize()
+        if time.monotonic() - t0 >= seconds:
+            break
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    return ev0.elapsed_time(ev1) / steps, steps, t0, t1
 
 
 def dist_setup(n_gpus):
@@ -287,6 +335,7 @@ def run_ours(args):
     sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                            else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     sampler.start()
+    sampler.wait_first()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -298,16 +347,32 @@ def run_ours(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    t_timed0 = time.monotonic()
     ev0.record(stream)
     for _ in range(args.steps):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
+    t_timed1 = time.monotonic()
     barrier(world)
     launches = lf.linformer_launch_count() - launches0
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
-    clocks = sampler.stop()
     ms_step = ms_total / args.steps
+
+    # --- clocks under load: a sustained pass of back-to-back forwards right after the
+    # timed steps (those last milliseconds, less than the sampling interval) -----------
+    sustained = None
+    if args.sustain_s > 0:
+        s_ms, s_steps, s_t0, s_t1 = sustained_pass(step, stream, args.sustain_s)
+        sustained = {"ms_per_step": s_ms, "steps": s_steps, "seconds": s_t1 - s_t0,
+                     "clocks": sampler.summary(s_t0, s_t1)}
+    sampler.stop()
+    timed_clocks = sampler.summary(t_timed0, t_timed1)
+    if sustained and sustained["clocks"]["samples"]:
+        clocks = dict(sustained["clocks"], window="sustained pass of back-to-back forwards "
+                      "directly after the timed steps", timed_region_samples=timed_clocks["samples"])
+    else:
+        clocks = dict(sampler.summary(), window="whole run")
     value = aggregate_throughput(w.tokens, ms_step, world)
 
     # --- per-kernel durations: a second pass of K steps with library events -----------
@@ -337,6 +402,9 @@ def run_ours(args):
                          "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak}
     dominant = max(kernels, key=lambda k: kernels[k]["avg_us"]) if kernels else None
+    mhz = clocks.get("sm_mhz")
+    for kd in kernels.values():  # clock-normalised duration, comparable across boxes
+        kd["kcycles_at_median_sm_clock"] = kd["avg_us"] * mhz / 1e3 if mhz else None
     traffic = None
     tfile = os.path.join(ROOT, "profiles", "traffic.json")
     if dominant and os.path.exists(tfile):
@@ -420,7 +488,7 @@ def run_ours(args):
             "path_roofline_frac_valid_rows": valid_frac,
             "l2_flushed": flushed,
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks,
+            "gpu_launches": launches, "clocks": clocks, "sustained": sustained,
         }
         print(json.dumps(line))
     if world > 1:
@@ -544,7 +612,8 @@ def run_backward(args):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop()
+    sampler.stop()
+    clocks = sampler.summary()
     launches = lf.linformer_launch_count() - launches0
     if lf.linformer_debug_read_device_status(stream) != 0:
         raise RuntimeError("device status set during the timed region")
@@ -696,6 +765,9 @@ def main():
                     help="units of the workload the CPU-baseline oracle pass covers")
     ap.add_argument("--ref-budget-s", type=float, default=90.0,
                     help="--impl reference: seconds for all warm-up + timed steps")
+    ap.add_argument("--sustain-s", type=float, default=2.0,
+                    help="seconds of back-to-back forwards after the timed steps, for the "
+                         "clock record (0: skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush-pass", action="store_true",

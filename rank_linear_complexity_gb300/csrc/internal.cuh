@@ -43,6 +43,16 @@ class KernelScope {
     cudaEvent_t a_ = nullptr, b_ = nullptr;
 };
 
+// Argument rules shared by the entry points (linformer_api.cu).
+bool aligned16(const void *p);
+int validate_common(int b, int h, int n, int d, int k, int share_mode, int dtype);
+int validate_f(int share_mode, const void *E, const void *F);
+// Null pointers, sizes, enums, the F rule and alignment of a forward call on device
+// buffers: LINFORMER_OK or the status the entry point returns.
+int validate_forward(const void *Q, const void *K, const void *V, const void *E, const void *F,
+                     const int32_t *pad_lengths, const void *O, int b, int h, int n, int d, int k,
+                     int share_mode, int dtype);
+
 // Device status word of the current device (set by bounded waits that ran out).
 int *device_status_ptr();
 
@@ -50,8 +60,11 @@ int *device_status_ptr();
 // whose freed memory stays mapped between calls (the device's default pool unmaps
 // freed memory at every synchronisation, and the next allocation maps it again).
 // Returns LINFORMER_OK or LINFORMER_ERR_ALLOC; free with workspace_free on a stream.
+// (workspace.cu: also the LINFORMER_FAIL_ALLOC and LINFORMER_WORKSPACE_GUARD switches.)
 int workspace_alloc(void **ptr, size_t bytes, cudaStream_t s);
 void workspace_free(void *ptr, cudaStream_t s);
+// The library's pool on device `dev` (created on first use), or nullptr.
+cudaMemPool_t library_pool(int dev);
 
 // Process-wide P.Vbar product-count setting (0 = automatic, 1, 2 or 3).
 int pv_terms_setting();

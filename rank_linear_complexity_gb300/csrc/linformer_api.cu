@@ -1,6 +1,6 @@
 // Host side of the C ABI declared in include/linformer_attn.h: argument
-// validation, path selection, stream-ordered workspace, launch bookkeeping,
-// profiling events and the device status word.
+// validation, path selection, launch bookkeeping, profiling events and the device
+// status word (the workspace pool is in workspace.cu).
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
@@ -32,55 +32,6 @@ std::vector<ProfileRecord> g_prof;
 constexpr int kMaxDevices = 64;
 int *g_status_addr[kMaxDevices] = {};
 std::mutex g_status_mu;
-
-// One memory pool per device for workspaces, created on first use, kept for the
-// process (release threshold: unlimited, so freed memory stays mapped).
-cudaMemPool_t g_pools[kMaxDevices] = {};
-std::mutex g_pool_mu;
-
-cudaMemPool_t library_pool(int dev) {
-    std::lock_guard<std::mutex> lock(g_pool_mu);
-    if (!g_pools[dev]) {
-        cudaMemPoolProps props{};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.handleTypes = cudaMemHandleTypeNone;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        cudaMemPool_t pool = nullptr;
-        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        uint64_t keep = ~uint64_t(0);
-        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-        g_pools[dev] = pool;
-    }
-    return g_pools[dev];
-}
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Shape, enum and F rules shared by every entry point.
-int validate_common(int b, int h, int n, int d, int k, int share_mode, int dtype) {
-    if (b < 1 || h < 1 || n < 1 || d < 1 || k < 1) return LINFORMER_ERR_SIZE;
-    if (share_mode < LINFORMER_SHARE_PER_HEAD || share_mode > LINFORMER_SHARE_LAYERWISE)
-        return LINFORMER_ERR_ENUM;
-    if (dtype < LINFORMER_F32 || dtype > LINFORMER_BF16_F32OUT) return LINFORMER_ERR_ENUM;
-    if (d > 128 || k > 1024) return LINFORMER_ERR_UNSUPPORTED;
-    const int64_t units = (int64_t)b * h;
-    if (units > (1LL << 31) - 1) return LINFORMER_ERR_SIZE;
-    if (units * (int64_t)n > (1LL << 40) || units * (int64_t)n * d > (1LL << 46))
-        return LINFORMER_ERR_SIZE;
-    return LINFORMER_OK;
-}
-
-int validate_f(int share_mode, const void *E, const void *F) {
-    const bool distinct = share_mode == LINFORMER_SHARE_PER_HEAD ||
-                          share_mode == LINFORMER_SHARE_HEADWISE;
-    if (distinct && !F) return LINFORMER_ERR_F_MODE;
-    if (!distinct && F && F != E) return LINFORMER_ERR_F_MODE;
-    return LINFORMER_OK;
-}
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
@@ -123,6 +74,43 @@ int run_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
 
 }  // namespace
 
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_common(int b, int h, int n, int d, int k, int share_mode, int dtype) {
+    if (b < 1 || h < 1 || n < 1 || d < 1 || k < 1) return LINFORMER_ERR_SIZE;
+    if (share_mode < LINFORMER_SHARE_PER_HEAD || share_mode > LINFORMER_SHARE_LAYERWISE)
+        return LINFORMER_ERR_ENUM;
+    if (dtype < LINFORMER_F32 || dtype > LINFORMER_BF16_F32OUT) return LINFORMER_ERR_ENUM;
+    if (d > 128 || k > 1024) return LINFORMER_ERR_UNSUPPORTED;
+    const int64_t units = (int64_t)b * h;
+    if (units > (1LL << 31) - 1) return LINFORMER_ERR_SIZE;
+    if (units * (int64_t)n > (1LL << 40) || units * (int64_t)n * d > (1LL << 46))
+        return LINFORMER_ERR_SIZE;
+    return LINFORMER_OK;
+}
+
+int validate_f(int share_mode, const void *E, const void *F) {
+    const bool distinct = share_mode == LINFORMER_SHARE_PER_HEAD ||
+                          share_mode == LINFORMER_SHARE_HEADWISE;
+    if (distinct && !F) return LINFORMER_ERR_F_MODE;
+    if (!distinct && F && F != E) return LINFORMER_ERR_F_MODE;
+    return LINFORMER_OK;
+}
+
+// Every argument rule of the forward entry points (device buffers).
+int validate_forward(const void *Q, const void *K, const void *V, const void *E, const void *F,
+                     const int32_t *pad_lengths, const void *O, int b, int h, int n, int d, int k,
+                     int share_mode, int dtype) {
+    if (!Q || !K || !V || !E || !O) return LINFORMER_ERR_NULL;
+    int st = validate_common(b, h, n, d, k, share_mode, dtype);
+    if (st) return st;
+    if ((st = validate_f(share_mode, E, F))) return st;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(E) || !aligned16(O) ||
+        (F && !aligned16(F)) || (reinterpret_cast<uintptr_t>(pad_lengths) & 3u))
+        return LINFORMER_ERR_ALIGN;
+    return LINFORMER_OK;
+}
+
 // Batch chunks of the host entry point's copy/compute pipeline.
 constexpr int kHostChunks = 8;
 
@@ -141,22 +129,6 @@ cudaStream_t side_stream(int i) {
     }
     return g_side[dev][i];
 }
-
-int workspace_alloc(void **ptr, size_t bytes, cudaStream_t s) {
-    int dev = 0;
-    cudaMemPool_t pool = nullptr;
-    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) pool = library_pool(dev);
-    const cudaError_t e =
-        pool ? cudaMallocFromPoolAsync(ptr, bytes, pool, s) : cudaMallocAsync(ptr, bytes, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        *ptr = nullptr;
-        return LINFORMER_ERR_ALLOC;
-    }
-    return LINFORMER_OK;
-}
-
-void workspace_free(void *ptr, cudaStream_t s) { cudaFreeAsync(ptr, s); }  // back to its pool
 
 KernelScope::KernelScope(int kernel_id, cudaStream_t s) : id_(kernel_id), s_(s) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -198,13 +170,9 @@ extern "C" int linformer_attn_fwd(const void *Q, const void *K, const void *V, c
                                   const void *F, const int32_t *pad_lengths, void *O, int b,
                                   int h, int n, int d, int k, int share_mode, int dtype,
                                   void *stream) {
-    if (!Q || !K || !V || !E || !O) return LINFORMER_ERR_NULL;
-    int st = validate_common(b, h, n, d, k, share_mode, dtype);
+    const int st = validate_forward(Q, K, V, E, F, pad_lengths, O, b, h, n, d, k, share_mode,
+                                    dtype);
     if (st) return st;
-    if ((st = validate_f(share_mode, E, F))) return st;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(E) || !aligned16(O) ||
-        (F && !aligned16(F)) || (reinterpret_cast<uintptr_t>(pad_lengths) & 3u))
-        return LINFORMER_ERR_ALIGN;
     Problem p{Q, K, V, E, F, pad_lengths, O, b, h, n, d, k, share_mode, dtype,
               as_stream(stream)};
     return run_forward(p, nullptr, nullptr);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "internal.cuh"
+
 namespace linformer {
 namespace tc {
 
@@ -170,6 +172,27 @@ struct AttnParams {
     int h, n, k, kpad, units, tiles_per_unit, forced_terms, out_fp32;
     float scale_log2;    // log2(e) / sqrt(d)
 };
+
+// The host's plan of one tensor-core forward: the projection's launch and the
+// workspace layout (images, split partials, per-unit counters + the product-count
+// summary word, per-unit info words, each piece rounded up to 256 bytes).
+struct ForwardPlan {
+    ProjPlan proj;
+    int64_t units, members, groups;
+    int kpad, mhalves, distinct, per_head, sms;
+    size_t img, part, cnt;
+    size_t bytes() const { return img + part + 2 * cnt; }
+};
+
+// Plans a forward of the validated problem p (tc_supported shapes) on the current
+// device.  part_budget: ~0 for a workspace sized to the plan; otherwise the size of a
+// fixed workspace, which must hold the images, counters and info words (else
+// LINFORMER_ERR_SIZE), the split partials taking what is left.
+int plan_forward(const Problem &p, size_t part_budget, ForwardPlan *f);
+// Launches the projection (writes Kbar/Vbar in fp32 and stops there when Kbar_out is
+// given) and the attention on p.stream, with the workspace ws of f.bytes() bytes.
+int run_forward(const Problem &p, const ForwardPlan &f, char *ws, float *Kbar_out,
+                float *Vbar_out);
 
 // threads: 128, or 256 for unsplit units without the fp32 Kbar/Vbar outputs.
 int launch_project(const CUtensorMap &tE, const CUtensorMap &tF, const CUtensorMap &tK,

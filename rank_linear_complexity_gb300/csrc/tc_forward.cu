@@ -67,111 +67,124 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
-int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
-    using namespace tc;
-    if (!encoder()) return LINFORMER_ERR_LAUNCH;
-    const int64_t units = p.units();
-    const int kpad = (p.k + 15) / 16 * 16;
-    const int mhalves = (kpad + 127) / 128;
-    const int distinct = p.distinct_f() ? 1 : 0;
-    const int per_head = p.proj_per_head() ? 1 : 0;
-    const int sms = sm_count();
-    const int64_t members = per_head ? p.b : units;
-    const ProjPlan plan = plan_projection(p.n, members, units / members, mhalves, distinct,
-                                          p.pad != nullptr, sms);
-    const int C = plan.C, CH = plan.CH;
-    if (plan.smem < 1024 + kProjectMinRing + 256) return LINFORMER_ERR_UNSUPPORTED;
+namespace tc {
 
-    // Workspace: images, split partials, per-unit counters (plus the product-count
-    // summary word after them) and info words.
-    const size_t img = up256(units * 4 * image_bytes(kpad));
-    const size_t part = up256(partial_bytes(units, C, mhalves));
-    const size_t cnt = up256((units + 1) * sizeof(int));
-    char *ws = nullptr;
-    if (workspace_alloc(reinterpret_cast<void **>(&ws), img + part + 2 * cnt, p.stream) !=
-        LINFORMER_OK)
-        return LINFORMER_ERR_ALLOC;
+int plan_forward(const Problem &p, size_t part_budget, ForwardPlan *fp) {
+    if (!encoder()) return LINFORMER_ERR_LAUNCH;
+    ForwardPlan f{};
+    f.units = p.units();
+    f.kpad = (p.k + 15) / 16 * 16;
+    f.mhalves = (f.kpad + 127) / 128;
+    f.distinct = p.distinct_f() ? 1 : 0;
+    f.per_head = p.proj_per_head() ? 1 : 0;
+    f.sms = sm_count();
+    f.members = f.per_head ? p.b : f.units;
+    f.groups = f.units / f.members;
+    f.img = up256(f.units * 4 * image_bytes(f.kpad));
+    f.cnt = up256((f.units + 1) * sizeof(int));  // + the product-count summary word
+    if (part_budget != ~size_t(0)) {  // a fixed workspace: images, counters and info first
+        if (f.img + 2 * f.cnt > part_budget) return LINFORMER_ERR_SIZE;
+        part_budget -= f.img + 2 * f.cnt;
+    }
+    f.proj = plan_projection(p.n, f.members, f.groups, f.mhalves, f.distinct, p.pad != nullptr,
+                             f.sms, part_budget);
+    if (f.proj.smem < 1024 + kProjectMinRing + 256) return LINFORMER_ERR_UNSUPPORTED;
+    if (f.proj.grid > 0x7fffffffLL) return LINFORMER_ERR_SIZE;
+    f.part = up256(partial_bytes(f.units, f.proj.C, f.mhalves));
+    *fp = f;
+    return LINFORMER_OK;
+}
+
+int run_forward(const Problem &p, const ForwardPlan &f, char *ws, float *Kbar_out,
+                float *Vbar_out) {
+    const int64_t units = f.units;
     uint8_t *images = reinterpret_cast<uint8_t *>(ws);
-    float *partial = C > 1 ? reinterpret_cast<float *>(ws + img) : nullptr;
-    int *counters = reinterpret_cast<int *>(ws + img + part);
-    int *info = reinterpret_cast<int *>(ws + img + part + cnt);
-    int st = LINFORMER_OK;
-    if (cudaMemsetAsync(counters, 0, cnt, p.stream) != cudaSuccess) st = LINFORMER_ERR_LAUNCH;
+    float *partial = f.proj.C > 1 ? reinterpret_cast<float *>(ws + f.img) : nullptr;
+    int *counters = reinterpret_cast<int *>(ws + f.img + f.part);
+    int *info = reinterpret_cast<int *>(ws + f.img + f.part + f.cnt);
+    // Counters and the product-count summary start at zero (also when the workspace
+    // is reused from an earlier call).
+    if (cudaMemsetAsync(counters, 0, f.cnt, p.stream) != cudaSuccess) return LINFORMER_ERR_LAUNCH;
 
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const uint64_t groups = per_head ? (uint64_t)p.h : 1;
+    const uint64_t groups = (uint64_t)f.groups;
     CUtensorMap tE, tF, tK, tV;
-    if (st == LINFORMER_OK &&
-        !(encode3d(&tE, p.E, bf, 2, p.n, p.k, groups, 64, 128 * mhalves) &&
-          encode3d(&tF, p.f_or_e(), bf, 2, p.n, p.k, groups, 64, 128 * mhalves) &&
+    if (!(encode3d(&tE, p.E, bf, 2, p.n, p.k, groups, 64, 128 * f.mhalves) &&
+          encode3d(&tF, p.f_or_e(), bf, 2, p.n, p.k, groups, 64, 128 * f.mhalves) &&
           encode3d(&tK, p.K, bf, 2, kD, p.n, units, 64, kBK) &&
           encode3d(&tV, p.V, bf, 2, kD, p.n, units, 64, kBK)))
-        st = LINFORMER_ERR_LAUNCH;
+        return LINFORMER_ERR_LAUNCH;
 
     int *status = device_status_ptr();
-    if (st == LINFORMER_OK) {
-        ProjParams pp{};
-        pp.pad = p.pad;
-        pp.partial = partial;
-        pp.images = images;
-        pp.counters = counters;
-        pp.terms_seen = counters + units;
-        pp.info = info;
-        pp.kbar_out = Kbar_out;
-        pp.vbar_out = Vbar_out;
-        pp.status = status;
-        pp.h = p.h;
-        pp.n = p.n;
-        pp.k = p.k;
-        pp.kpad = kpad;
-        pp.mhalves = mhalves;
-        pp.C = C;
-        pp.CH = CH;
-        pp.stages = plan.stages;
-        pp.stages2 = plan.stages2;
-        pp.pairs = plan.pairs;
-        pp.prefetch = project_prefetch(CH);
-        pp.prefetch_proj = project_prefetch_proj((size_t)groups * p.k * p.n * 2 * (1 + distinct));
-        pp.distinct = distinct;
-        pp.per_head = per_head;
-        pp.members = (int)members;
-        pp.forced_terms = pv_terms_setting();
-        st = plan.grid > 0x7fffffffLL
-                 ? LINFORMER_ERR_SIZE
-                 : launch_project(tE, tF, tK, tV, pp, (int)plan.grid,
-                                  Kbar_out ? 128 : plan.threads, plan.smem, p.stream);
-    }
+    ProjParams pp{};
+    pp.pad = p.pad;
+    pp.partial = partial;
+    pp.images = images;
+    pp.counters = counters;
+    pp.terms_seen = counters + units;
+    pp.info = info;
+    pp.kbar_out = Kbar_out;
+    pp.vbar_out = Vbar_out;
+    pp.status = status;
+    pp.h = p.h;
+    pp.n = p.n;
+    pp.k = p.k;
+    pp.kpad = f.kpad;
+    pp.mhalves = f.mhalves;
+    pp.C = f.proj.C;
+    pp.CH = f.proj.CH;
+    pp.stages = f.proj.stages;
+    pp.stages2 = f.proj.stages2;
+    pp.pairs = f.proj.pairs;
+    pp.prefetch = project_prefetch(f.proj.CH);
+    pp.prefetch_proj =
+        project_prefetch_proj((size_t)groups * p.k * p.n * 2 * (1 + f.distinct));
+    pp.distinct = f.distinct;
+    pp.per_head = f.per_head;
+    pp.members = (int)f.members;
+    pp.forced_terms = pv_terms_setting();
+    int st = launch_project(tE, tF, tK, tV, pp, (int)f.proj.grid,
+                            Kbar_out ? 128 : f.proj.threads, f.proj.smem, p.stream);
+    if (st != LINFORMER_OK || Kbar_out) return st;
 
-    if (st == LINFORMER_OK && !Kbar_out) {
-        CUtensorMap tQ, tO;
-        const bool f32out = p.dtype == LINFORMER_BF16_F32OUT;
-        if (!(encode3d(&tQ, p.Q, bf, 2, kD, p.n, units, 64, kTileM) &&
-              (f32out ? encode3d(&tO, p.O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, p.n, units, 32,
-                                 kTileM)
-                      : encode3d(&tO, p.O, bf, 2, kD, p.n, units, 64, kTileM)))) {
-            st = LINFORMER_ERR_LAUNCH;
-        } else {
-            AttnParams ap{};
-            ap.pad = p.pad;
-            ap.out = p.O;
-            ap.images = images;
-            ap.info = info;
-            ap.terms_seen = counters + units;
-            ap.status = status;
-            ap.h = p.h;
-            ap.n = p.n;
-            ap.k = p.k;
-            ap.kpad = kpad;
-            ap.units = (int)units;
-            ap.tiles_per_unit = (p.n + kTileM - 1) / kTileM;
-            ap.forced_terms = pv_terms_setting();
-            ap.out_fp32 = f32out ? 1 : 0;
-            ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
-            const int64_t tiles = units * ap.tiles_per_unit;
-            const int grid = (int)std::min<int64_t>(sms, tiles);
-            st = launch_attend(tQ, tO, ap, grid, p.stream);
-        }
-    }
+    CUtensorMap tQ, tO;
+    const bool f32out = p.dtype == LINFORMER_BF16_F32OUT;
+    if (!(encode3d(&tQ, p.Q, bf, 2, kD, p.n, units, 64, kTileM) &&
+          (f32out ? encode3d(&tO, p.O, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, p.n, units, 32,
+                             kTileM)
+                  : encode3d(&tO, p.O, bf, 2, kD, p.n, units, 64, kTileM))))
+        return LINFORMER_ERR_LAUNCH;
+    AttnParams ap{};
+    ap.pad = p.pad;
+    ap.out = p.O;
+    ap.images = images;
+    ap.info = info;
+    ap.terms_seen = counters + units;
+    ap.status = status;
+    ap.h = p.h;
+    ap.n = p.n;
+    ap.k = p.k;
+    ap.kpad = f.kpad;
+    ap.units = (int)units;
+    ap.tiles_per_unit = (p.n + kTileM - 1) / kTileM;
+    ap.forced_terms = pp.forced_terms;
+    ap.out_fp32 = f32out ? 1 : 0;
+    ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
+    const int64_t tiles = units * ap.tiles_per_unit;
+    const int grid = (int)std::min<int64_t>(f.sms, tiles);
+    return launch_attend(tQ, tO, ap, grid, p.stream);
+}
+
+}  // namespace tc
+
+int tc_forward(const Problem &p, float *Kbar_out, float *Vbar_out) {
+    tc::ForwardPlan f;
+    int st = tc::plan_forward(p, ~size_t(0), &f);
+    if (st != LINFORMER_OK) return st;
+    char *ws = nullptr;
+    if (workspace_alloc(reinterpret_cast<void **>(&ws), f.bytes(), p.stream) != LINFORMER_OK)
+        return LINFORMER_ERR_ALLOC;
+    st = tc::run_forward(p, f, ws, Kbar_out, Vbar_out);
     workspace_free(ws, p.stream);
     return st;
 }

@@ -16,7 +16,9 @@ CUDA_INC = "/usr/local/cuda/include"
 def test_projection_plans_respect_the_kernel_limits(tmp_path):
     exe = tmp_path / "projection_plan_check"
     src = os.path.join(HERE, "host", "projection_plan_check.cc")
-    subprocess.run(["g++", "-std=c++17", "-O1", "-x", "c++", "-I", CUDA_INC, src, "-o", str(exe)],
+    inc = os.path.join(os.path.dirname(HERE), "include")
+    subprocess.run(["g++", "-std=c++17", "-O1", "-x", "c++", "-I", CUDA_INC, "-I", inc, src,
+                    "-o", str(exe)],
                    check=True, capture_output=True, text=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0, out.stdout + out.stderr

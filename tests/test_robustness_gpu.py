@@ -1,0 +1,186 @@
+"""Robustness checks that need no GPU fault: a forced workspace-allocation failure,
+guard rows around the output and after every workspace, and the invariance of the
+output under a permutation of the projected positions.
+
+* Allocation failure: with LINFORMER_FAIL_ALLOC=1 every workspace allocation of the
+  library fails; each entry point must return LINFORMER_ERR_ALLOC (-7) before it
+  launches anything, and leave its output untouched.
+* Guard rows: O is a view into a larger buffer with guard rows before and after it,
+  all filled with a pattern; after the call the guards must be unchanged.  With
+  LINFORMER_WORKSPACE_GUARD=1 the library also puts 4 KB of a pattern after each
+  workspace and checks it when the workspace is freed (a changed byte sets the device
+  status word).  Shapes cover the tile edges of both kernels (n around multiples of
+  128 and 64, k around multiples of 16 and 32), every sharing mode and output type.
+* Permutation: the method sums over the k projected positions inside the softmax
+  and in P.Vbar, so permuting the rows of E and F together ("Linformer 요약 설명",
+  section Model: row j of E merges the n positions into compressed position j)
+  cannot change O beyond rounding.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import rank_linear_complexity_gb300.linformer as lf
+from oracle import oracle as orc
+from rank_linear_complexity_gb300.workloads import (BF16, BF16_F32OUT, F32, HEADWISE, KV,
+                                                    LAYERWISE, PER_HEAD, output_gradient)
+from tests.parity import case_inputs, check, host64, to_device
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+ERR_ALLOC = -7
+
+
+@pytest.fixture
+def env(monkeypatch):
+    return monkeypatch
+
+
+def _out_dtype(dtype):
+    return torch.bfloat16 if dtype == BF16 else torch.float32
+
+
+# --- forced allocation failure ---------------------------------------------------------
+
+ALLOC_CASES = [
+    # (b, h, n, d, k, mode, dtype): tensor-core path, fp32 SIMT path, bf16 SIMT path (whose
+    # projection alone needs no workspace: linformer_project_fwd is not checked there)
+    (2, 3, 256, 64, 128, LAYERWISE, BF16),
+    (2, 2, 200, 64, 48, PER_HEAD, F32),
+    (1, 2, 300, 32, 40, KV, BF16),
+]
+
+
+@pytest.mark.parametrize("case", ALLOC_CASES, ids=[f"n{c[2]}d{c[3]}k{c[4]}t{c[6]}"
+                                                   for c in ALLOC_CASES])
+def test_forced_allocation_failure_returns_before_launch(env, case):
+    b, h, n, d, k, mode, dtype = case
+    g = to_device(case_inputs(b, h, n, d, k, mode, dtype, seed=3), DEV)
+    O = torch.full((b, h, n, d), float("nan"), dtype=_out_dtype(dtype), device=DEV)
+    torch.cuda.synchronize()
+    env.setenv("LINFORMER_FAIL_ALLOC", "1")
+    launches = lf.linformer_launch_count()
+    st = lf.linformer_attn_fwd(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], O,
+                               b, h, n, d, k, mode, dtype)
+    assert st == ERR_ALLOC, lf.status_string(st)
+    if dtype == F32 or lf.linformer_select_path(b, h, n, d, k, mode, dtype) == lf.PATH_TENSOR:
+        Kb = torch.empty((b, h, k, d), dtype=torch.float32, device=DEV)
+        st = lf.linformer_project_fwd(g["K"], g["V"], g["E"], g["F"], g["lengths"], Kb,
+                                      torch.empty_like(Kb), b, h, n, d, k, mode, dtype)
+        assert st == ERR_ALLOC
+    pin = {kk: (v.cpu().pin_memory() if v is not None else None) for kk, v in g.items()}
+    Oh = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    st = lf.linformer_attn_fwd_host(pin["Q"], pin["K"], pin["V"], pin["E"], pin["F"],
+                                    pin["lengths"], Oh, b, h, n, d, k, mode, dtype)
+    assert st == ERR_ALLOC
+    assert lf.linformer_launch_count() == launches  # nothing was launched
+    torch.cuda.synchronize()
+    assert torch.isnan(O.float()).all()  # O untouched
+    env.delenv("LINFORMER_FAIL_ALLOC")
+    st = lf.linformer_attn_fwd(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], O,
+                               b, h, n, d, k, mode, dtype)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert lf.linformer_debug_read_device_status() == 0
+
+
+def test_forced_allocation_failure_backward_and_dense(env):
+    b, h, n, d, k = 1, 2, 128, 64, 32
+    g = to_device(case_inputs(b, h, n, d, k, PER_HEAD, F32, seed=4), DEV)
+    dO = output_gradient(b, h, n, d, seed=5).to(DEV)
+    out = [torch.empty_like(g[c]) for c in ("Q", "K", "V", "E", "F")]
+    env.setenv("LINFORMER_FAIL_ALLOC", "1")
+    launches = lf.linformer_launch_count()
+    st = lf.linformer_attn_bwd(g["Q"], g["K"], g["V"], g["E"], g["F"], None, dO, *out,
+                               b, h, n, d, k, PER_HEAD, F32)
+    assert st == ERR_ALLOC
+    st = lf.linformer_dense_attn_fwd(g["Q"], g["K"], g["V"], None, out[0], b, h, n, d, F32)
+    assert st == ERR_ALLOC
+    assert lf.linformer_launch_count() == launches
+
+
+# --- guard rows --------------------------------------------------------------------------
+
+GUARD_ROWS = 8
+GUARD_CASES = [
+    # (b, h, n, k, mode, dtype, lengths)
+    (2, 3, 8, 16, LAYERWISE, BF16, None),
+    (2, 2, 127, 255, PER_HEAD, BF16, None),
+    (1, 3, 128, 256, KV, BF16_F32OUT, None),
+    (3, 2, 129, 200, HEADWISE, BF16, [129, 1, 64]),
+    (2, 2, 640, 96, PER_HEAD, BF16, [640, 333]),
+    (2, 2, 136, 33, KV, F32, [136, 70]),
+    (2, 2, 250, 64, LAYERWISE, BF16, [250, 129]),        # n % 8 != 0: SIMT path
+    (16, 12, 520, 256, LAYERWISE, BF16, None),           # two-unit projection CTAs
+    (1, 4, 4096, 128, HEADWISE, BF16, None),             # split sequence: partial sums
+]
+
+
+@pytest.mark.parametrize("case", GUARD_CASES, ids=[f"b{c[0]}n{c[2]}k{c[3]}m{c[4]}t{c[5]}"
+                                                   for c in GUARD_CASES])
+def test_guard_rows_around_output_and_workspace(env, case):
+    b, h, n, k, mode, dtype, lengths = case
+    d = 64
+    x = case_inputs(b, h, n, d, k, mode, dtype, seed=7 + n, lengths=lengths)
+    g = to_device(x, DEV)
+    odt = _out_dtype(dtype)
+    rows = b * h * n
+    buf = torch.empty((rows + 2 * GUARD_ROWS, d), dtype=odt, device=DEV)
+    buf.view(torch.uint8 if odt == torch.bfloat16 else torch.int32).fill_(
+        0x5A if odt == torch.bfloat16 else 0x5A5A5A5A)
+    before = buf.clone()
+    O = buf[GUARD_ROWS:GUARD_ROWS + rows].view(b, h, n, d)
+    assert O.data_ptr() % 16 == 0
+    env.setenv("LINFORMER_WORKSPACE_GUARD", "1")
+    st = lf.linformer_attn_fwd(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], O,
+                               b, h, n, d, k, mode, dtype)
+    assert st == 0, lf.status_string(st)
+    torch.cuda.synchronize()
+    assert lf.linformer_debug_read_device_status() == 0  # workspace guards intact
+    assert torch.equal(buf[:GUARD_ROWS], before[:GUARD_ROWS])
+    assert torch.equal(buf[GUARD_ROWS + rows:], before[GUARD_ROWS + rows:])
+    check(host64(O), orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                       mode)[0], dtype, str(case))
+
+
+def test_guard_rows_around_projection_outputs(env):
+    b, h, n, d, k = 2, 3, 1000, 64, 200
+    x = case_inputs(b, h, n, d, k, PER_HEAD, BF16, ragged=True, seed=8)
+    g = to_device(x, DEV)
+    rows = b * h * k
+    bufs = [torch.full((rows + 2 * GUARD_ROWS, d), -7.25, device=DEV) for _ in range(2)]
+    Kb, Vb = (bb[GUARD_ROWS:GUARD_ROWS + rows].view(b, h, k, d) for bb in bufs)
+    env.setenv("LINFORMER_WORKSPACE_GUARD", "1")
+    st = lf.linformer_project_fwd(g["K"], g["V"], g["E"], g["F"], g["lengths"], Kb, Vb,
+                                  b, h, n, d, k, PER_HEAD, BF16)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert lf.linformer_debug_read_device_status() == 0
+    for bb in bufs:
+        assert (bb[:GUARD_ROWS] == -7.25).all() and (bb[GUARD_ROWS + rows:] == -7.25).all()
+
+
+# --- permutation of the projected positions ------------------------------------------------
+
+@pytest.mark.parametrize("mode,dtype,k", [(PER_HEAD, BF16, 256), (KV, BF16, 200),
+                                          (HEADWISE, BF16_F32OUT, 128), (LAYERWISE, BF16, 64),
+                                          (PER_HEAD, F32, 96)])
+def test_permuting_projected_positions_on_gpu(mode, dtype, k):
+    b, h, n = 2, 3, 776 if dtype != F32 else 300
+    x = case_inputs(b, h, n, 64, k, mode, dtype, ragged=True, seed=90 + k)
+    perm = torch.from_numpy(np.random.default_rng(k).permutation(k))
+    y = dict(x)
+    y["E"] = x["E"].index_select(-2, perm).contiguous()
+    if x["F"] is not None:
+        y["F"] = x["F"].index_select(-2, perm).contiguous()
+    outs = []
+    for inp in (x, y):
+        gi = to_device(inp, DEV)
+        outs.append(lf.attention(gi["Q"], gi["K"], gi["V"], gi["E"], gi["F"], gi["lengths"],
+                                 mode, out_fp32=(dtype == BF16_F32OUT)))
+    torch.cuda.synchronize()
+    ref = orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"], mode)[0]
+    check(host64(outs[1]), ref, dtype, "permuted E/F against the unpermuted oracle")
+    check(host64(outs[0]), ref, dtype, "unpermuted")

@@ -483,6 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(s_full + 10);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     TileRanges *ranges = reinterpret_cast<TileRanges *>(s_full + 11);
+    // One per MMA-issuing thread (scores, P.V half a, P.V half b): a final commit that
+    // lets the thread wait for its own products before the CTA frees TMEM, also when
+    // a wait elsewhere gave up.
+    uint64_t *drain = s_full + 15;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t img_bytes = (uint32_t)p.kpad * kRowBytes;
@@ -504,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(o_full + s, 2);     // both P.V threads
             mbar_init(tmem_free + s, 4);  // one arrival per epilogue warp
         }
+        for (int i = 0; i < 3; ++i) mbar_init(drain + i, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tQ);
@@ -599,6 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ++j;
                 }
+                mma_commit(drain);
+                mbar_wait_drain(drain, 0);
             }
             __syncwarp();
         } else if (warp >= kPvWarp) {
@@ -659,6 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(o_full + w);
                     ++j;
                 }
+                mma_commit(drain + 1 + h);
+                mbar_wait_drain(drain + 1 + h, 0);
                 if (h == 0 && nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1);  // no copy outlives the CTA
             }
             __syncwarp();

@@ -141,9 +141,12 @@ inline ProjPlan plan_projection(int n, int64_t members, int64_t groups, int mhal
     return pl;
 }
 
-// The projection's split reduction reuses the ring for two 32 KB slice buffers.
-// Every plan above gives a ring of at least 96 KB.
-constexpr size_t kProjectMinRing = 64 * 1024;
+// After the main loop the projection reuses its ring: the split reduction's two 32 KB
+// slice buffers at [0, 64 KB) and, in four-warp launches, a 32 KB image staging buffer
+// at [64 KB, 96 KB); eight-warp launches stage in [0, 128 KB) (two groups, two buffers
+// each).  Every plan above gives at least 96 KB, and 192 KB to eight-warp launches.
+constexpr size_t kProjectMinRing = 96 * 1024;
+constexpr size_t kProjectMinRingWide = 128 * 1024;
 
 struct ProjParams {
     const int32_t *pad;

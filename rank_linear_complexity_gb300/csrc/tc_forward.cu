@@ -88,7 +88,9 @@ int plan_forward(const Problem &p, size_t part_budget, ForwardPlan *fp) {
     }
     f.proj = plan_projection(p.n, f.members, f.groups, f.mhalves, f.distinct, p.pad != nullptr,
                              f.sms, part_budget);
-    if (f.proj.smem < 1024 + kProjectMinRing + 256) return LINFORMER_ERR_UNSUPPORTED;
+    if (f.proj.smem < 1024 + kProjectMinRing + 256 ||
+        (f.proj.threads == 256 && f.proj.smem < 1024 + kProjectMinRingWide + 256))
+        return LINFORMER_ERR_UNSUPPORTED;
     if (f.proj.grid > 0x7fffffffLL) return LINFORMER_ERR_SIZE;
     f.part = up256(partial_bytes(f.units, f.proj.C, f.mhalves));
     *fp = f;

@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
         const uint32_t idesc64 = idesc_f16(128, 64, 1, 0, 1);
         if (lane == 0) {
             bool ok = true;
+            int issued = 0;  // stages whose products were issued
             for (int it = 0; it < nkb; ++it) {
                 const int s = it % S;
                 if (!mbar_wait(full + s, (it / S) & 1, p.status, 13, abort_flag)) {
@@ -243,11 +244,16 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                     }
                 }
                 mma_commit(empty + s);
+                issued = it + 1;
             }
-            if (ok && nkb > 0)
+            // The accumulators are final (or, after an abort, every product issued has
+            // finished) when acc_full completes: the epilogue and the TMEM release wait
+            // for it.
+            if (issued > 0)
                 mma_commit(acc_full);
             else
                 mbar_arrive(acc_full);
+            (void)ok;
         }
         __syncwarp();
     }
@@ -264,7 +270,34 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
         // Eight warps (launched only for unsplit units, E = F): warps 0-3 write the
         // Kbar images while warps 4-7 find max|Vbar| and write the Vbar images.  The
         // accumulators are final in TMEM; rows past k are zero there (so are E's).
+        // Each group puts one M-half of its two images (hi and lo, 16 KB each) into
+        // shared memory in the images' own layout, and one of its threads copies them
+        // out with two bulk stores: whole lines, where a warp's 16-byte stores would
+        // touch 32 lines each.  The ring is idle now; each group double-buffers its
+        // steps in its own 64 KB of it.
         const bool vgroup = warp >= 4;
+        const int gt = tid & 127;              // thread within the group
+        // the group's named barrier (literal ids, so that the compiler sees which ones)
+        auto gsync = [&]() {
+            if (vgroup) named_barrier_sync(3, 128);
+            else named_barrier_sync(2, 128);
+        };
+        int step = 0;                          // M-halves staged by this group so far
+        auto claim = [&]() -> uint8_t * {      // staging buffer of this step, once free
+            if (gt == 0 && step >= 2) bulk_wait_read1();
+            gsync();
+            return smem + (vgroup ? 65536 : 0) + 32768 * (step & 1);
+        };
+        auto flush = [&](uint8_t *stg, uint8_t *img_hi, uint8_t *img_lo, int mh, int rows) {
+            fence_proxy_async_smem();
+            gsync();
+            if (gt == 0) {
+                bulk_store(img_hi + (size_t)mh * 16384, stg, (uint32_t)rows * kRowBytes);
+                bulk_store(img_lo + (size_t)mh * 16384, stg + 16384, (uint32_t)rows * kRowBytes);
+                bulk_commit();
+            }
+            ++step;
+        };
 #pragma unroll 1
         for (int us = 0; us < nunits && !aborted; ++us) {
             const int uu = us ? u_b : u;
@@ -273,26 +306,28 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
             if (!vgroup) {
 #pragma unroll 1
                 for (int mh = 0; mh < p.mhalves; ++mh) {
-                    const int j = mh * 128 + jl;
+                    const int rows = min(128, p.kpad - 128 * mh);
                     uint32_t v[64];
                     tmem_ld64(lane_base + mh * 128 * nunits + ucol, v);
-                    if (j >= p.kpad) continue;
+                    uint8_t *stg = claim();
+                    if (jl < rows) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        uint32_t hi[4], lo[4];
+                        for (int q = 0; q < 8; ++q) {
+                            uint32_t hi[4], lo[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x0 = __uint_as_float(v[q * 8 + 2 * e]);
-                            const float x1 = __uint_as_float(v[q * 8 + 2 * e + 1]);
-                            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-                            const float2 hf = __bfloat1622float2(h);  // exact
-                            hi[e] = *reinterpret_cast<const uint32_t *>(&h);
-                            lo[e] = pack_bf16(x0 - hf.x, x1 - hf.y);
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 = __uint_as_float(v[q * 8 + 2 * e]);
+                                const float x1 = __uint_as_float(v[q * 8 + 2 * e + 1]);
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                                const float2 hf = __bfloat1622float2(h);  // exact
+                                hi[e] = *reinterpret_cast<const uint32_t *>(&h);
+                                lo[e] = pack_bf16(x0 - hf.x, x1 - hf.y);
+                            }
+                            *image_chunk(stg, jl, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         }
-                        *image_chunk(img, j, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *image_chunk(img + image_bytes(p.kpad), j, q) =
-                            make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
+                    flush(stg, img, img + image_bytes(p.kpad), mh, rows);
                 }
             } else {
                 float vmax = 0.f;
@@ -317,27 +352,28 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                                       : (vmax < kOneTermMaxV ? 1 : (vmax < kTwoTermMaxV ? 2 : 3));
 #pragma unroll 1
                 for (int mh = 0; mh < p.mhalves; ++mh) {
-                    const int j = mh * 128 + jl;
+                    const int rows = min(128, p.kpad - 128 * mh);
                     uint32_t v[64];
                     tmem_ld64(lane_base + mh * 128 * nunits + ucol + 64, v);
-                    if (j >= p.kpad) continue;
+                    uint8_t *stg = claim();
+                    if (jl < rows) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        uint32_t hi[4], lo[4];
+                        for (int q = 0; q < 8; ++q) {
+                            uint32_t hi[4], lo[4];
 #pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
-                            const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
-                            const __half2 h = __floats2half2_rn(x0, x1);
-                            const float2 hf = __half22float2(h);  // exact
-                            hi[e2] = *reinterpret_cast<const uint32_t *>(&h);
-                            lo[e2] = pack_f16(x0 - hf.x, x1 - hf.y);
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
+                                const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
+                                const __half2 h = __floats2half2_rn(x0, x1);
+                                const float2 hf = __half22float2(h);  // exact
+                                hi[e2] = *reinterpret_cast<const uint32_t *>(&h);
+                                lo[e2] = pack_f16(x0 - hf.x, x1 - hf.y);
+                            }
+                            *image_chunk(stg, jl, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         }
-                        *image_chunk(img + 2 * image_bytes(p.kpad), j, q) =
-                            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *image_chunk(img + 3 * image_bytes(p.kpad), j, q) =
-                            make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
+                    flush(stg, img + 2 * image_bytes(p.kpad), img + 3 * image_bytes(p.kpad), mh, rows);
                 }
                 if (jl == 0) {
                     p.info[uu] = pack_info(terms, e);
@@ -347,6 +383,7 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                 named_barrier_sync(1, 128);  // red[] is reused by the next unit
             }
         }
+        if (gt == 0) bulk_wait0();  // the images are written before the CTA exits
     } else {
     if (!aborted && Cu > 1) {
         // This chunk's sums, [half of k_pad][column][row]: a warp stores 128 contiguous bytes.
@@ -368,6 +405,28 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
         __syncthreads();
     }
 
+    // Images leave through shared memory: all 128 threads put one M-half of two images
+    // (hi and lo, 16 KB each) at [64 KB, 96 KB) of the idle ring, in the images' own
+    // layout (the split reduction's slice buffers take [0, 64 KB)), and thread 0 copies
+    // them out with two bulk stores (whole lines rather than 16-byte pieces of 32 rows
+    // per store instruction).
+    int staged = 0;  // bulk groups thread 0 has committed
+    auto stage_claim = [&]() -> uint8_t * {
+        if (tid == 0 && staged > 0) bulk_wait_read0();
+        __syncthreads();
+        return smem + 65536;
+    };
+    auto stage_flush = [&](uint8_t *stg, uint8_t *img_hi, uint8_t *img_lo, int mh) {
+        const int rows = min(128, p.kpad - 128 * mh);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store(img_hi + (size_t)mh * 16384, stg, (uint32_t)rows * kRowBytes);
+            bulk_store(img_lo + (size_t)mh * 16384, stg + 16384, (uint32_t)rows * kRowBytes);
+            bulk_commit();
+        }
+        ++staged;
+    };
     // Images, info word and product count of each unit of the CTA (a pair of units
     // only ever comes unsplit).
 #pragma unroll 1
@@ -437,7 +496,8 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 64; ++i) acc[i] = 0.f;
                 }
-                if (half == 0) {  // Kbar: bf16 hi + bf16 lo images
+                if (half == 0) {  // Kbar: bf16 hi + bf16 lo images, staged (see stage_claim)
+                    uint8_t *stg = stage_claim();
                     if (j < p.kpad) {
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
@@ -456,11 +516,11 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                                     o[1] = hf.y + __bfloat162float(__float2bfloat16_rn(r1));
                                 }
                             }
-                            *image_chunk(img, j, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            *image_chunk(img + image_bytes(p.kpad), j, q) =
-                                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                            *image_chunk(stg, jl, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         }
                     }
+                    stage_flush(stg, img, img + image_bytes(p.kpad), mh);
                 } else {  // Vbar: max|Vbar| first; the images need the unit-wide scale
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -497,30 +557,31 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
             const int j = mh * 128 + jl;
             uint32_t v[64];
             tmem_ld64(lane_base + mh * 128 * nunits + ucol + 64, v);
-            if (j >= p.kpad) continue;
+            uint8_t *stg = stage_claim();
+            if (j < p.kpad) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint32_t hi[4], lo[4];
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
-                    const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
-                    const __half2 h = __floats2half2_rn(x0, x1);
-                    const float2 hf = __half22float2(h);  // exact
-                    const float r0 = x0 - hf.x, r1 = x1 - hf.y;
-                    hi[e2] = *reinterpret_cast<const uint32_t *>(&h);
-                    lo[e2] = pack_f16(r0, r1);
-                    if (kOut && p.vbar_out && j < p.k) {
-                        float *o = p.vbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e2;
-                        o[0] = (hf.x + __half2float(__float2half_rn(r0))) / vscale;
-                        o[1] = (hf.y + __half2float(__float2half_rn(r1))) / vscale;
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
+                        const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
+                        const __half2 h = __floats2half2_rn(x0, x1);
+                        const float2 hf = __half22float2(h);  // exact
+                        const float r0 = x0 - hf.x, r1 = x1 - hf.y;
+                        hi[e2] = *reinterpret_cast<const uint32_t *>(&h);
+                        lo[e2] = pack_f16(r0, r1);
+                        if (kOut && p.vbar_out && j < p.k) {
+                            float *o = p.vbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e2;
+                            o[0] = (hf.x + __half2float(__float2half_rn(r0))) / vscale;
+                            o[1] = (hf.y + __half2float(__float2half_rn(r1))) / vscale;
+                        }
                     }
+                    *image_chunk(stg, jl, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
-                *image_chunk(img + 2 * image_bytes(p.kpad), j, q) =
-                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *image_chunk(img + 3 * image_bytes(p.kpad), j, q) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
+            stage_flush(stg, img + 2 * image_bytes(p.kpad), img + 3 * image_bytes(p.kpad), mh);
         }
         if (tid == 0 && ok) {
             p.info[uu] = pack_info(terms, e);
@@ -529,6 +590,7 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
         }
             __syncthreads();  // red[] is reused by the next unit
     }
+    if (tid == 0 && staged > 0) bulk_wait0();  // the images are written before the CTA exits
     }  // four-warp epilogue
     tc_fence_before();
     __syncthreads();

@@ -45,7 +45,9 @@ int main() {
         CHECK(partial_bytes(units, p.C, mh) <= budget || p.C == 1, "partials within budget");
         CHECK(p.stages >= 2 && p.stages <= 6, "ring depth in [2, 6]");
         CHECK(p.smem <= 227 * 1024, "shared memory within one CTA's limit");
-        CHECK(p.smem >= 1024 + kProjectMinRing + 256, "ring holds the reduction's slices");
+        CHECK(p.smem >= 1024 + kProjectMinRing + 256, "ring holds the reduction's slices and staging");
+        CHECK(p.threads != 256 || p.smem >= 1024 + kProjectMinRingWide + 256,
+              "eight-warp launches: ring holds both groups' staging buffers");
         CHECK(p.smem >= 1024 + project_stage_bytes(mh, dist, 1) * p.stages + 256,
               "one-unit ring fits");
         CHECK(p.pairs >= 0 && p.pairs <= members / 2, "at most members / 2 pairs");

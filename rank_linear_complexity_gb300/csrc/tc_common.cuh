@@ -20,7 +20,8 @@ constexpr int kBK = 64;          // sequence rows per projection pipeline stage
 // already in the 128-byte-swizzled shared-memory layout the attention kernel's
 // MMAs read (16-byte chunk q of row j sits at chunk position q ^ (j % 8)):
 //   0: Kbar hi (bf16)   1: Kbar lo (bf16)   2: Vbar hi (fp16)   3: Vbar lo (fp16)
-// Vbar is stored scaled by 2^-e (e >= 0 keeps it inside the fp16 range).
+// Vbar is stored scaled by 2^-e (e >= 0 keeps it inside the fp16 range).  Image 3 is
+// written only for units that take two or more P.Vbar products (the only readers).
 __host__ __device__ inline size_t image_bytes(int kpad) { return (size_t)kpad * kRowBytes; }
 
 // info word per unit: bits 0-7 = number of P.Vbar products (1, 2 or 3), bits 8-15 = e.

@@ -293,7 +293,8 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
             gsync();
             if (gt == 0) {
                 bulk_store(img_hi + (size_t)mh * 16384, stg, (uint32_t)rows * kRowBytes);
-                bulk_store(img_lo + (size_t)mh * 16384, stg + 16384, (uint32_t)rows * kRowBytes);
+                if (img_lo)
+                    bulk_store(img_lo + (size_t)mh * 16384, stg + 16384, (uint32_t)rows * kRowBytes);
                 bulk_commit();
             }
             ++step;
@@ -370,10 +371,13 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                                 lo[e2] = pack_f16(x0 - hf.x, x1 - hf.y);
                             }
                             *image_chunk(stg, jl, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                            if (terms >= 2)
+                                *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         }
                     }
-                    flush(stg, img + 2 * image_bytes(p.kpad), img + 3 * image_bytes(p.kpad), mh, rows);
+                    // Vbar lo is read only by units with two or more P.Vbar products.
+                    flush(stg, img + 2 * image_bytes(p.kpad),
+                          terms >= 2 ? img + 3 * image_bytes(p.kpad) : nullptr, mh, rows);
                 }
                 if (jl == 0) {
                     p.info[uu] = pack_info(terms, e);
@@ -422,7 +426,8 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
         __syncthreads();
         if (tid == 0) {
             bulk_store(img_hi + (size_t)mh * 16384, stg, (uint32_t)rows * kRowBytes);
-            bulk_store(img_lo + (size_t)mh * 16384, stg + 16384, (uint32_t)rows * kRowBytes);
+            if (img_lo)
+                bulk_store(img_lo + (size_t)mh * 16384, stg + 16384, (uint32_t)rows * kRowBytes);
             bulk_commit();
         }
         ++staged;
@@ -578,10 +583,13 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                         }
                     }
                     *image_chunk(stg, jl, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    if (terms >= 2)
+                        *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
-            stage_flush(stg, img + 2 * image_bytes(p.kpad), img + 3 * image_bytes(p.kpad), mh);
+            // Vbar lo is read only by units with two or more P.Vbar products.
+            stage_flush(stg, img + 2 * image_bytes(p.kpad),
+                        terms >= 2 ? img + 3 * image_bytes(p.kpad) : nullptr, mh);
         }
         if (tid == 0 && ok) {
             p.info[uu] = pack_info(terms, e);

@@ -1,5 +1,5 @@
-// Backward of the Linformer attention forward in fp32 (SIMT): the gradients of O with
-// respect to Q, K, V, E and F given dO.  The forward is the definition in "Linformer
+// Backward of the Linformer attention forward in fp32: the gradients of O with respect
+// to Q, K, V, E and F given dO.  The forward is the definition in "Linformer
 // (Self-Attention with Linear Complexity) 요약 설명", section Model (Kbar = E.K,
 // Vbar = F.V, E and F of shape k x n; rows t >= L of K and V count as zero and query
 // rows i >= L give O = 0, padding paragraph), with the scaled dot product; the pages
@@ -11,9 +11,12 @@
 //   dK = E^T dKbar, dV = F^T dVbar (rows >= L zero)
 //   dE = sum over the units sharing E of dKbar K^T (+ dVbar V^T when F is E), dF alike,
 //   with the columns t >= L of each unit's term zero.
-// Every product, Kbar and Vbar included, runs on the batched SIMT matrix product of
-// simt_gemm.cu (split over the sequence for the four k x d results that sum over it);
-// two kernels here do the softmax backward rows and the sums over sharing groups.
+// Every product, Kbar and Vbar included, runs on the batched tensor-core product of
+// tc_gemm.cu (fp32 operands split into bf16 hi + lo, three products, fp32 accumulation):
+// split over the sequence for the four k x d results that sum over it; with k <= 256
+// the softmax and the softmax backward in the epilogues of the products that make S and
+// dP (else the row softmax of simt_gemm.cu and the row kernel here); dE and dF as sums
+// over units inside the product, in chunks of units whose partials are then added.
 #include "simt_gemm.cuh"
 
 namespace linformer {
@@ -34,24 +37,6 @@ __global__ void softmax_bwd_rows_kernel(const float *P, float *dP, int k, long l
     for (int j = lane; j < k; j += 32) g[j] = p[j] * (g[j] - dsum);
 }
 
-// out[m] = sum over the units sharing matrix m of per_unit[unit] (k x n each), in unit
-// order; per_head: matrix m = head, units b*h + m; else one matrix for all units.
-__global__ void group_sum_kernel(const float *per_unit, float *out, int b, int h, int per_head,
-                                 long long elems) {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int groups = per_head ? h : 1;
-    if (i >= elems * groups) return;
-    const int m = (int)(i / elems);
-    const long long e = i % elems;
-    float acc = 0.f;
-    if (per_head) {
-        for (int bi = 0; bi < b; ++bi) acc += per_unit[((long long)bi * h + m) * elems + e];
-    } else {
-        for (long long z = 0; z < (long long)b * h; ++z) acc += per_unit[z * elems + e];
-    }
-    out[i] = acc;
-}
-
 }  // namespace
 
 int simt_backward(const Problem &p, const float *dO, float *dQ, float *dK, float *dV, float *dE,
@@ -60,17 +45,16 @@ int simt_backward(const Problem &p, const float *dO, float *dQ, float *dK, float
     const bool per_head = p.proj_per_head(), distinct = p.distinct_f();
     const long long kd = (long long)k * d, nk = (long long)n * k, nd = (long long)n * d,
                     kn = (long long)k * n;
-    // split-K partials of the four k x d products that sum over the sequence
     const int sms = sm_count();
-    const size_t bytes = sizeof(float) * ((size_t)units * (4 * kd + 2 * nk + kn * (distinct ? 2 : 1)) +
-                                          (size_t)kMaxSplits * units * kd);
+    // Kbar, Vbar, dKbar, dVbar, P, dS, and the split-K partials of the k x d products
+    const size_t part_floats = (size_t)kMaxSplits * units * kd;
+    const size_t bytes = sizeof(float) * ((size_t)units * (4 * kd + 2 * nk) + part_floats);
     void *ws = nullptr;
     if (workspace_alloc(&ws, bytes, p.stream) != LINFORMER_OK) return LINFORMER_ERR_ALLOC;
     float *Kb = static_cast<float *>(ws), *Vb = Kb + units * kd;
-    float *P = Vb + units * kd, *dS = P + units * nk;
-    float *dKb = dS + units * nk, *dVb = dKb + units * kd;
-    float *gE = dVb + units * kd, *gF = distinct ? gE + units * kn : gE;
-    float *part = gF + units * kn;
+    float *dKb = Vb + units * kd, *dVb = dKb + units * kd;
+    float *P = dVb + units * kd, *dS = P + units * nk;
+    float *part = dS + units * nk;
     const float *Q = static_cast<const float *>(p.Q), *K = static_cast<const float *>(p.K),
                 *V = static_cast<const float *>(p.V), *E = static_cast<const float *>(p.E),
                 *F = static_cast<const float *>(p.f_or_e());
@@ -82,47 +66,67 @@ int simt_backward(const Problem &p, const float *dO, float *dQ, float *dK, float
         return GemmArgs{A, B, C, sC, ldc, M, N, K_, alpha, beta, p.pad, h, n, mrows, mcols,
                         1, 0, nullptr};
     };
+    // Row forms fused into the products' epilogues while a tile holds whole rows
+    const bool fused = k <= 256;
     // Kbar = E K, Vbar = F V over rows t < L
-    int st = project_f32(p, Kb, Vb, part, LINFORMER_KERNEL_BACKWARD);
-    // S = Q Kbar^T / sqrt(d), then P (rows >= L zero)
-    if (!st) st = batched_gemm(args(opA(Q, nd, d, 0, kPerUnit), opB(Kb, kd, d, 1, kPerUnit), P, nk, k, n, k,
-                            d, scale, 0.f, 0, 0), units, s);
-    const long long rows = (long long)units * n;
-    const unsigned rblocks = (unsigned)((rows + 7) / 8);
-    if (!st) st = softmax_rows(P, p.pad, h, n, k, units, 0, s);
-    // dP = dO Vbar^T, then dS in place
-    if (!st) st = batched_gemm(args(opA(dO, nd, d, 0, kPerUnit, 1), opB(Vb, kd, d, 1, kPerUnit), dS, nk, k,
-                            n, k, d, 1.f, 0.f, 0, 0), units, s);
-    if (!st) {
+    int st = project_f32(p, Kb, Vb, part, LINFORMER_KERNEL_BACKWARD, true);
+    // P = softmax(Q Kbar^T / sqrt(d)) (rows >= L zero)
+    GemmArgs gs = args(opA(Q, nd, d, 0, kPerUnit), opB(Kb, kd, d, 1, kPerUnit), P, nk, k, n, k, d,
+                       scale, 0.f, 0, 0);
+    if (fused) gs.epi = kEpiSoftmax;
+    if (!st) st = tc_batched_gemm(gs, units, s, nullptr, 0, sms);
+    if (!st && !fused) st = softmax_rows(P, p.pad, h, n, k, units, 0, s);
+    // dP = dO Vbar^T, dS = P * (dP - rowsum(P * dP))
+    GemmArgs gp = args(opA(dO, nd, d, 0, kPerUnit, 1), opB(Vb, kd, d, 1, kPerUnit), dS, nk, k, n, k,
+                       d, 1.f, 0.f, 0, 0);
+    if (fused) {
+        gp.epi = kEpiSoftmaxBwd;
+        gp.aux = P;
+    }
+    if (!st) st = tc_batched_gemm(gp, units, s, nullptr, 0, sms);
+    if (!st && !fused) {
+        const long long rows = (long long)units * n;
         KernelScope scope(LINFORMER_KERNEL_BACKWARD, s);
-        softmax_bwd_rows_kernel<<<rblocks, 256, 0, s>>>(P, dS, k, rows);
+        softmax_bwd_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(P, dS, k, rows);
         if (cudaPeekAtLastError() != cudaSuccess) st = LINFORMER_ERR_LAUNCH;
     }
     // dVbar = P^T dO; dQ = dS Kbar / sqrt(d); dKbar = dS^T Q / sqrt(d)
-    if (!st) st = batched_gemm(args(opA(P, nk, k, 1, kPerUnit), opB(dO, nd, d, 0, kPerUnit, 1), dVb, kd, d,
-                            k, d, n, 1.f, 0.f, 0, 0), units, s, part, kMaxSplits, sms);
-    if (!st) st = batched_gemm(args(opA(dS, nk, k, 0, kPerUnit), opB(Kb, kd, d, 0, kPerUnit), dQ, nd, d, n,
-                            d, k, scale, 0.f, 1, 0), units, s);
-    if (!st) st = batched_gemm(args(opA(dS, nk, k, 1, kPerUnit), opB(Q, nd, d, 0, kPerUnit, 1), dKb, kd, d,
-                            k, d, n, scale, 0.f, 0, 0), units, s, part, kMaxSplits, sms);
+    if (!st) st = tc_batched_gemm(args(opA(P, nk, k, 1, kPerUnit), opB(dO, nd, d, 0, kPerUnit, 1), dVb,
+                                       kd, d, k, d, n, 1.f, 0.f, 0, 0),
+                                  units, s, part, part_floats, sms);
+    if (!st) st = tc_batched_gemm(args(opA(dS, nk, k, 0, kPerUnit), opB(Kb, kd, d, 0, kPerUnit), dQ, nd,
+                                       d, n, d, k, scale, 0.f, 1, 0),
+                                  units, s, nullptr, 0, sms);
+    if (!st) st = tc_batched_gemm(args(opA(dS, nk, k, 1, kPerUnit), opB(Q, nd, d, 0, kPerUnit, 1), dKb,
+                                       kd, d, k, d, n, scale, 0.f, 0, 0),
+                                  units, s, part, part_floats, sms);
     // dK = E^T dKbar, dV = F^T dVbar (rows >= L zero)
-    if (!st) st = batched_gemm(args(opA(E, kn, n, 1, pidx), opB(dKb, kd, d, 0, kPerUnit), dK, nd, d, n, d, k,
-                            1.f, 0.f, 1, 0), units, s);
-    if (!st) st = batched_gemm(args(opA(F, kn, n, 1, pidx), opB(dVb, kd, d, 0, kPerUnit), dV, nd, d, n, d, k,
-                            1.f, 0.f, 1, 0), units, s);
-    // per-unit E (and F) terms, columns t >= L zero, then the sums over sharing groups
-    if (!st) st = batched_gemm(args(opA(dKb, kd, d, 0, kPerUnit), opB(K, nd, d, 1, kPerUnit, 2), gE, kn, n,
-                            k, n, d, 1.f, 0.f, 0, 1), units, s);
-    if (!st) st = batched_gemm(args(opA(dVb, kd, d, 0, kPerUnit), opB(V, nd, d, 1, kPerUnit, 2), gF, kn, n,
-                            k, n, d, 1.f, distinct ? 0.f : 1.f, 0, 1), units, s);
-    const long long groups = per_head ? h : 1;
-    const unsigned gblocks = (unsigned)((groups * kn + 255) / 256);
-    if (!st) {
-        KernelScope scope(LINFORMER_KERNEL_BACKWARD, s);
-        group_sum_kernel<<<gblocks, 256, 0, s>>>(gE, dE, p.b, h, per_head ? 1 : 0, kn);
-        if (distinct) group_sum_kernel<<<gblocks, 256, 0, s>>>(gF, dF, p.b, h, per_head ? 1 : 0, kn);
-        if (cudaPeekAtLastError() != cudaSuccess) st = LINFORMER_ERR_LAUNCH;
-    }
+    if (!st) st = tc_batched_gemm(args(opA(E, kn, n, 1, pidx), opB(dKb, kd, d, 0, kPerUnit), dK, nd, d,
+                                       n, d, k, 1.f, 0.f, 1, 0),
+                                  units, s, nullptr, 0, sms);
+    if (!st) st = tc_batched_gemm(args(opA(F, kn, n, 1, pidx), opB(dVb, kd, d, 0, kPerUnit), dV, nd, d,
+                                       n, d, k, 1.f, 0.f, 1, 0),
+                                  units, s, nullptr, 0, sms);
+    // dE (and dF) = the sum over the units sharing the matrix of dKbar K^T (dVbar V^T),
+    // columns t >= L of each unit's term zero; P and dS, no longer needed, hold the
+    // partial sums.
+    const int groups = per_head ? h : 1, per_group = per_head ? p.b : units;
+    auto grad = [&](float *out, const float *dX, const float *X, const float *dX2,
+                    const float *X2) {
+        GemmArgs g = args(opA(dX, kd, d, 0, kPerUnit), opB(X, nd, d, 1, kPerUnit, 2), out, kn, n, k,
+                          n, d, 1.f, 0.f, 0, 0);
+        g.usum_groups = groups;
+        g.usum_per_group = per_group;
+        g.usum_ga = per_head ? 1 : 0;
+        g.usum_gb = per_head ? h : 1;
+        if (dX2) {
+            g.A2 = opA(dX2, kd, d, 0, kPerUnit);
+            g.B2 = opB(X2, nd, d, 1, kPerUnit, 2);
+        }
+        return tc_batched_gemm(g, units, s, P, (size_t)2 * units * nk, sms);
+    };
+    if (!st) st = distinct ? grad(dE, dKb, K, nullptr, nullptr) : grad(dE, dKb, K, dVb, V);
+    if (!st && distinct) st = grad(dF, dVb, V, nullptr, nullptr);
     workspace_free(ws, s);
     return st;
 }

@@ -250,6 +250,15 @@ int launch_gemm(const GemmArgs &g, int units, cudaStream_t s, int kernel_id) {
 
 }  // namespace
 
+int launch_splitk_reduce(const GemmArgs &g, int units, cudaStream_t s, int kernel_id) {
+    const long long total = (long long)units * g.M * g.N;
+    KernelScope scope(kernel_id, s);
+    splitk_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(g, units);
+    return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
+}
+
+void set_operand_vec(Operand &o, int contiguous_extent) { set_vec(o, contiguous_extent); }
+
 int batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, int max_splits, int sms,
                  int kernel_id) {
     set_vec(g.A, g.A.xfast ? g.M : g.K);
@@ -285,7 +294,8 @@ int softmax_rows(float *S, const int32_t *pad, int h, int rows_per_unit, int col
     return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
 }
 
-int project_f32(const Problem &p, float *Kbar, float *Vbar, float *part, int kernel_id) {
+int project_f32(const Problem &p, float *Kbar, float *Vbar, float *part, int kernel_id,
+                bool tensor) {
     const int units = (int)p.units(), n = p.n, d = p.d, k = p.k;
     const long long kd = (long long)k * d, nd = (long long)n * d, kn = (long long)k * n;
     const int pidx = p.proj_per_head() ? kPerHead : kShared;
@@ -294,12 +304,17 @@ int project_f32(const Problem &p, float *Kbar, float *Vbar, float *part, int ker
     const float *E = static_cast<const float *>(p.E), *F = static_cast<const float *>(p.f_or_e());
     GemmArgs g{opA(E, kn, n, 0, pidx), opB(K, nd, d, 0, kPerUnit, 1), Kbar, kd, d, k, d, n, 1.f,
                0.f, p.pad, p.h, n, 0, 0, 1, 0, nullptr};
-    int st = batched_gemm(g, units, p.stream, part, kMaxSplits, sms, kernel_id);
+    auto product = [&](const GemmArgs &a) {
+        return tensor ? tc_batched_gemm(a, units, p.stream, part,
+                                        (size_t)kMaxSplits * units * kd, sms, kernel_id)
+                      : batched_gemm(a, units, p.stream, part, kMaxSplits, sms, kernel_id);
+    };
+    int st = product(g);
     if (st) return st;
     g.A = opA(F, kn, n, 0, pidx);
     g.B = opB(V, nd, d, 0, kPerUnit, 1);
     g.C = Vbar;
-    return batched_gemm(g, units, p.stream, part, kMaxSplits, sms, kernel_id);
+    return product(g);
 }
 
 int attend_f32(const Problem &p, const float *Kbar, const float *Vbar, float *P,

@@ -43,7 +43,23 @@ struct GemmArgs {
     // (M x N, dense) and a second kernel forms C.  Set by batched_gemm.
     int splits, kchunk;
     float *part;
+    int *status;  // device status word for bounded waits that run out (tensor-core kernel)
+    // Tensor-core product only (tc_batched_gemm):
+    int epi = 0;                 // an EpilogueKind
+    const float *aux = nullptr;  // kEpiSoftmaxBwd: P, laid out as C
+    // usum_groups > 0: a sum over units.  Output matrix g < usum_groups (C + g sC) is the
+    // sum over i < usum_per_group of A_u B_u (+ A2_u B2_u when A2.p is set), unit
+    // u = g usum_ga + i usum_gb, each term with its own unit's length masks; the
+    // output masks must be off.
+    int usum_groups = 0, usum_per_group = 0, usum_ga = 0, usum_gb = 0;
+    Operand A2{}, B2{};
 };
+
+// What the tensor-core product writes: alpha A B (+ beta C, output masks), the row
+// softmax of alpha A B (rows at or past the unit's length zero), or
+// aux * (alpha A B - rowsum(aux * alpha A B)) (the softmax backward with aux = P).
+// The two row forms need N <= 256 (a tile holds whole rows) and no sum over units.
+enum EpilogueKind { kEpiPlain = 0, kEpiSoftmax = 1, kEpiSoftmaxBwd = 2 };
 
 // Operand A (M x K) or B (K x N) of a product from a stored row-major matrix: `trans`
 // says the stored matrix is the operand's transpose; nmask 1 zeroes operand rows >= L,
@@ -65,6 +81,23 @@ inline Operand opB(const float *p, long long stride, int ld, int trans, int inde
 int batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part = nullptr,
                  int max_splits = 1, int sms = 0, int kernel_id = LINFORMER_KERNEL_BACKWARD);
 
+// The same product on the tensor cores (tc_gemm.cu): fp32 operands are split into bf16
+// hi + lo parts on the way into shared memory and C = A_hi B_hi + A_hi B_lo + A_lo B_hi
+// accumulates in fp32 (the dropped A_lo B_lo and the split's residual are about 2^-18
+// of each term), with the epilogue forms and sums over units of GemmArgs.  With `part`
+// (part_floats floats) a plain product may split K (a sum over units, its units) for
+// about four work items per SM; partials are added in split order.  Returns
+// LINFORMER_OK, LINFORMER_ERR_SIZE (a row form with N > 256 or a sum, mismatched second
+// operands) or LINFORMER_ERR_LAUNCH.
+int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part = nullptr,
+                    size_t part_floats = 0, int sms = 0,
+                    int kernel_id = LINFORMER_KERNEL_BACKWARD);
+
+// C = the sum over splits of g.part (+ beta C), with the output masks (split order).
+int launch_splitk_reduce(const GemmArgs &g, int units, cudaStream_t s, int kernel_id);
+// Sets o.vec: whether 4-element groups along o's contiguous axis may be 16-byte loads.
+void set_operand_vec(Operand &o, int contiguous_extent);
+
 // Row softmax in place over S (units x rows_per_unit rows of `cols` values): rows
 // i >= L are written as zero; with mask_cols, columns j >= L take no part (p = 0).
 int softmax_rows(float *S, const int32_t *pad, int h, int rows_per_unit, int cols,
@@ -76,8 +109,10 @@ int softmax_rows(float *S, const int32_t *pad, int h, int rows_per_unit, int col
 constexpr int kMaxSplits = 8;
 
 // Kbar = Ehat K and Vbar = Fhat V over the rows t < L for fp32 inputs, as two split
-// products; `part` holds kMaxSplits * units * k * d floats.
-int project_f32(const Problem &p, float *Kbar, float *Vbar, float *part, int kernel_id);
+// products (on the tensor cores with `tensor`); `part` holds kMaxSplits * units * k * d
+// floats.
+int project_f32(const Problem &p, float *Kbar, float *Vbar, float *part, int kernel_id,
+                bool tensor = false);
 
 // O = softmax(Q Kbar^T / sqrt(d)) Vbar for fp32 Q and O, query rows i >= L zero, as
 // two products around the row softmax; `P` holds units * n * k floats.

@@ -1,0 +1,734 @@
+// Batched fp32 matrix products on the tensor cores (declared in simt_gemm.cuh):
+// C_z = alpha A_z B_z + beta C_z over units z, with the operand conventions of
+// batched_gemm (each operand a row-major matrix of its unit, of its head, or shared,
+// read as stored or transposed, with rows or columns at or past the unit's sequence
+// length read as zero), and two further forms the backward of the Linformer attention
+// needs ("Linformer(Self-Attention with Linear Complexity) 요약 설명", section Model:
+// the forward's definition; the gradients are its chain rule):
+//   - a fused epilogue: C = the row softmax of alpha A B (P from the scores), or
+//     C = Paux * (alpha A B - rowsum(Paux * alpha A B)) (dS from dP), the tile holding
+//     whole rows;
+//   - a sum over units: output matrix g = sum over the units u of its group of A_u B_u
+//     (+ A2_u B2_u), the gradient of a projection matrix shared by those units.
+//
+// fp32 precision from bf16 tensor-core products: every operand element a is split
+// as a_hi = bf16(a), a_lo = bf16(a - a_hi) (|a - a_hi - a_lo| <= 2^-18 |a|), and
+// C = A_hi B_hi + A_hi B_lo + A_lo B_hi in fp32 (the dropped A_lo B_lo term is at most
+// 2^-18 of each product term).
+//
+// Persistent and warp-specialized: one CTA per SM walks the work items (a 128 x BN
+// output tile of one unit, or of one split of its K range, or of one chunk of a group
+// of units) in a fixed order, and three roles run through that order concurrently:
+//   - eight producer warps read the fp32 tiles of A (128 x 64) and B (64 x BN) of each
+//     64-deep step from global memory, coalesced along each operand's contiguous axis,
+//     split them and write hi and lo into a ring of shared-memory stages in the
+//     128-byte-swizzled layout the MMA reads (K-major when the operand's K axis is
+//     contiguous in memory, MN-major when its M or N axis is); with BN = 64 the loads of
+//     the next step are in flight while the current one is split and stored;
+//   - one thread issues the twelve MMAs of a step (four 16-deep slices, three products
+//     each) into one of two TMEM accumulators of BN fp32 columns, the tiles alternating;
+//   - four epilogue warps (TMEM lane quarters 0..3) drain the other accumulator through
+//     a small shared-memory transpose, so that every fp32 store of C (or of a split's
+//     partial) is a whole 128-byte line.
+// So the loads of later steps, the products and the stores of earlier tiles overlap.
+// Every wait is bounded (the status word gets 31..34 and the roles stop).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "simt_gemm.cuh"
+#include "sm100_ptx.cuh"
+
+namespace linformer {
+namespace simt {
+namespace {
+
+using namespace ptx;
+
+constexpr int kTM = 128;                 // output rows per tile
+constexpr int kTK = 64;                  // K per step (one 128-byte row of bf16)
+constexpr int kProducerWarps = 8;
+constexpr int kProducers = kProducerWarps * 32;
+constexpr int kEpilogueWarp0 = kProducerWarps;  // warps 8..11: lane quarters 0..3
+constexpr int kMmaWarp = kProducerWarps + 4;     // warp 12
+constexpr int kThreads = (kMmaWarp + 1) * 32;    // 416
+constexpr int kPitch = 33;                       // floats per row of a warp's transpose
+static_assert(kEpilogueWarp0 % 4 == 0, "epilogue warp w reads TMEM lanes 32 (w % 4) ..");
+
+// Stages of the ring (192 KB of operand tiles for every BN) and the shared memory in all.
+template <int BN>
+struct Cfg {
+    static constexpr int kStages = BN == 64 ? 4 : (BN == 128 ? 3 : 2);
+    static constexpr uint32_t kA = kTM * kTK * 2, kB = BN * kTK * 2;  // one hi (or lo) tile
+    static constexpr uint32_t kStage = 2 * kA + 2 * kB;
+    static constexpr uint32_t kRing = kStages * kStage;
+    static constexpr uint32_t kTranspose = 4 * 32 * kPitch * 4;
+    static constexpr uint32_t kTmemCols = 2 * BN;  // 128, 256 or 512: a power of two
+    static constexpr size_t kSmem = 1024 + kRing + kTranspose + 256;
+    static constexpr bool kPrefetch = false;      // two steps of loads in flight
+};
+
+__device__ __forceinline__ int tc_unit_length(const int32_t *pad, int unit, int h, int n) {
+    if (!pad) return n;
+    const int L = pad[unit / h];
+    return L < 0 ? 0 : (L > n ? n : L);
+}
+
+// Byte offset of the 8-byte group of 4 elements starting at (x, k) of an X x 64 tile:
+// K-major (row x of 128 bytes holds k = 0..63; k a multiple of 4) or MN-major (row k
+// of each 64-wide x block holds x .. x + 63, blocks 8 KB apart; x a multiple of 4).
+// 16-byte chunk c of row r sits at chunk position c ^ (r % 8).
+__device__ __forceinline__ uint32_t kmajor_off(int x, int k) {
+    return (uint32_t)(x * 128 + ((((k * 2) >> 4) ^ (x & 7)) << 4) + ((k * 2) & 15));
+}
+__device__ __forceinline__ uint32_t mnmajor_off(int x, int k) {
+    const int xi = x & 63;
+    return (uint32_t)((x >> 6) * (kTK * 128) + k * 128 + ((((xi * 2) >> 4) ^ (k & 7)) << 4) +
+                      ((xi * 2) & 15));
+}
+
+// hi and lo bf16 parts of four values, as two 8-byte words.
+__device__ __forceinline__ void split4(float4 f, uint2 &hi, uint2 &lo) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(f.x, f.y), h1 = __floats2bfloat162_rn(f.z, f.w);
+    const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);  // exact
+    const __nv_bfloat162 l0 = __floats2bfloat162_rn(f.x - f0.x, f.y - f0.y);
+    const __nv_bfloat162 l1 = __floats2bfloat162_rn(f.z - f1.x, f.w - f1.y);
+    hi = make_uint2(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1));
+    lo = make_uint2(*reinterpret_cast<const uint32_t *>(&l0), *reinterpret_cast<const uint32_t *>(&l1));
+}
+
+// A producer thread's share of one BX x 64 operand tile: groups of four consecutive
+// elements along the stored matrix's contiguous axis.  Along x (xfast): BX / 4 threads
+// cover one k row, group g of thread t is at x = 4 (t % (BX / 4)), k = t / (BX / 4) +
+// g (1024 / BX).  Along k: 16 threads cover one x row, x = t / 16 + 16 g, k = 4 (t % 16).
+template <int BX>
+struct Frag {
+    static constexpr int kGroups = BX * kTK / 4 / kProducers;
+    static constexpr int kRowThreads = BX / 4;                 // xfast: threads per k row
+    static constexpr int kKRowsPerGroup = kProducers / kRowThreads;
+    float4 v[kGroups];
+};
+
+// Issues the loads of tile (x0 .., k0 ..) of matrix m.  Elements out of range (x >= X,
+// k >= K) or masked (x or k at or past the unit's length L, per the operand's masks)
+// are zero.  A tile wholly inside and unmasked (the usual case) is read with one 16-byte
+// load per group from a per-thread base address; otherwise each group is checked, and
+// a wholly valid one is still one 16-byte load when the operand allows it.
+template <int BX>
+__device__ __forceinline__ void frag_load(Frag<BX> &f, const Operand &o, const float *m, int x0,
+                                          int k0, int X, int K, int L, int tid) {
+    using F = Frag<BX>;
+    const bool inside = o.vec && x0 + BX <= X && k0 + kTK <= K && (!o.mask_x || x0 + BX <= L) &&
+                        (!o.mask_k || k0 + kTK <= L);
+    if (inside) {
+        const float *p;
+        long long step;
+        if (o.xfast) {
+            p = m + (long long)(k0 + tid / F::kRowThreads) * o.ld + x0 + (tid % F::kRowThreads) * 4;
+            step = (long long)F::kKRowsPerGroup * o.ld;
+        } else {
+            p = m + (long long)(x0 + tid / 16) * o.ld + k0 + (tid % 16) * 4;
+            step = 16LL * o.ld;
+        }
+#pragma unroll
+        for (int g = 0; g < F::kGroups; ++g) f.v[g] = __ldg(reinterpret_cast<const float4 *>(p + g * step));
+        return;
+    }
+#pragma unroll
+    for (int g = 0; g < F::kGroups; ++g) {
+        const int x = o.xfast ? x0 + (tid % F::kRowThreads) * 4 : x0 + tid / 16 + 16 * g;
+        const int k = o.xfast ? k0 + tid / F::kRowThreads + g * F::kKRowsPerGroup : k0 + (tid % 16) * 4;
+        const long long base = o.xfast ? (long long)k * o.ld + x : (long long)x * o.ld + k;
+        bool in[4];
+        bool all = true;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int xe = o.xfast ? x + e : x, ke = o.xfast ? k : k + e;
+            in[e] = xe < X && ke < K && !(o.mask_x && xe >= L) && !(o.mask_k && ke >= L);
+            all = all && in[e];
+        }
+        if (all && o.vec) {
+            f.v[g] = __ldg(reinterpret_cast<const float4 *>(m + base));
+        } else {
+            f.v[g].x = in[0] ? __ldg(m + base) : 0.f;
+            f.v[g].y = in[1] ? __ldg(m + base + 1) : 0.f;
+            f.v[g].z = in[2] ? __ldg(m + base + 2) : 0.f;
+            f.v[g].w = in[3] ? __ldg(m + base + 3) : 0.f;
+        }
+    }
+}
+
+// Splits the loaded groups and writes hi and lo into their tiles.  The swizzle phase
+// of a group's row (row % 8) is the same for all of a thread's groups except along x
+// with BX = 256, where it alternates.
+template <int BX>
+__device__ __forceinline__ void frag_store(const Frag<BX> &f, int xfast, uint8_t *hi, uint8_t *lo,
+                                           int tid) {
+    using F = Frag<BX>;
+    if (xfast) {
+        const int xr = (tid % F::kRowThreads) * 4, kr0 = tid / F::kRowThreads;
+#pragma unroll
+        for (int g = 0; g < F::kGroups; ++g) {
+            uint2 h, l;
+            split4(f.v[g], h, l);
+            const uint32_t off = mnmajor_off(xr, kr0 + g * F::kKRowsPerGroup);
+            *reinterpret_cast<uint2 *>(hi + off) = h;
+            *reinterpret_cast<uint2 *>(lo + off) = l;
+        }
+    } else {
+        const uint32_t off0 = kmajor_off(tid / 16, (tid % 16) * 4);
+#pragma unroll
+        for (int g = 0; g < F::kGroups; ++g) {
+            uint2 h, l;
+            split4(f.v[g], h, l);
+            const uint32_t off = off0 + (uint32_t)g * 16u * 128u;  // 16 rows on, same phase
+            *reinterpret_cast<uint2 *>(hi + off) = h;
+            *reinterpret_cast<uint2 *>(lo + off) = l;
+        }
+    }
+}
+
+// Shared-memory descriptor of a tile and its advance per 16-deep K slice.  K-major:
+// 8-row groups 1 KB apart, +32 bytes a slice (inside the swizzle atom).  MN-major:
+// 64-wide x blocks 8 KB apart, 8-row (k) groups 1 KB apart, +2 KB a slice.
+__device__ __forceinline__ uint64_t tile_desc(const uint8_t *t, int mn) {
+    return sdesc(smem_u32(t), mn ? kTK * 128 : 16, 1024, kSwizzle128B);
+}
+__device__ __forceinline__ uint64_t slice_step(int mn) { return mn ? 128u : 2u; }
+
+// The work items of one launch, in the order every role walks them: item w is tile
+// row mt = w % tiles_m of tile column nt = (w / tiles_m) % tiles_n, of split (or unit
+// chunk) sp and output matrix z (a unit, or a group of units in a sum).
+struct Sched {
+    int tiles_m, tiles_n, splits, zcount;
+    long long items;
+    int ksteps;              // 64-deep steps of one unit's whole K
+    int usum;                // 1: z is a group; its terms i < per_group are units g * ga + i * gb
+    int per_group, ga, gb, uc, terms;  // chunks of uc units; terms 2 with A2 B2
+};
+
+struct Item {
+    int z, row0, col0, split, nk;
+    int kbeg, kend, first;   // K range (plain) or first unit term of the chunk (sum)
+};
+
+template <int BN>
+__device__ __forceinline__ Item item_at(const GemmArgs &g, const Sched &sc, long long w) {
+    Item it;
+    const int mt = (int)(w % sc.tiles_m);
+    w /= sc.tiles_m;
+    const int nt = (int)(w % sc.tiles_n);
+    w /= sc.tiles_n;
+    it.split = (int)(w % sc.splits);
+    it.z = (int)(w / sc.splits);
+    it.row0 = mt * kTM;
+    it.col0 = nt * BN;
+    if (sc.usum) {
+        it.first = it.split * sc.uc;
+        const int cnt = min(sc.per_group - it.first, sc.uc);
+        it.nk = cnt > 0 ? cnt * sc.terms * sc.ksteps : 0;
+        it.kbeg = 0;
+        it.kend = g.K;
+    } else {
+        it.first = 0;
+        it.kbeg = it.split * g.kchunk;
+        it.kend = min(g.K, it.kbeg + g.kchunk);
+        it.nk = it.kend > it.kbeg ? (it.kend - it.kbeg + kTK - 1) / kTK : 0;
+    }
+    return it;
+}
+
+// Step s of item `it`: the operands, the unit they are read for, and the K window.
+struct StepSrc {
+    Operand a, b;
+    int unit, k0, kend;
+};
+__device__ __forceinline__ StepSrc step_src(const GemmArgs &g, const Sched &sc, const Item &it,
+                                            int s) {
+    StepSrc r;
+    if (sc.usum) {
+        const int per_unit = sc.terms * sc.ksteps;
+        const int i = it.first + s / per_unit, rem = s % per_unit;
+        const int term = rem / sc.ksteps;
+        r.unit = it.z * sc.ga + i * sc.gb;
+        r.k0 = (rem % sc.ksteps) * kTK;
+        r.kend = g.K;
+        r.a = term ? g.A2 : g.A;
+        r.b = term ? g.B2 : g.B;
+    } else {
+        r.unit = it.z;
+        r.k0 = it.kbeg + s * kTK;
+        r.kend = it.kend;
+        r.a = g.A;
+        r.b = g.B;
+    }
+    return r;
+}
+
+// The producers' position in the walk: item w (its decoded form) and step s in it.
+template <int BN>
+struct Cursor {
+    long long w;
+    int s;
+    Item it;
+    __device__ __forceinline__ bool valid(const Sched &sc) const { return w < sc.items; }
+    // Moves to the next step, skipping items without steps.
+    __device__ __forceinline__ void skip_empty(const GemmArgs &g, const Sched &sc) {
+        while (w < sc.items && s >= it.nk) {
+            w += gridDim.x;
+            s = 0;
+            if (w < sc.items) it = item_at<BN>(g, sc, w);
+        }
+    }
+    __device__ __forceinline__ void start(const GemmArgs &g, const Sched &sc) {
+        w = blockIdx.x;
+        s = 0;
+        if (w < sc.items) it = item_at<BN>(g, sc, w);
+        skip_empty(g, sc);
+    }
+    __device__ __forceinline__ void next(const GemmArgs &g, const Sched &sc) {
+        ++s;
+        skip_empty(g, sc);
+    }
+};
+
+template <int BN>
+__device__ __forceinline__ void load_step(Frag<kTM> &fa, Frag<BN> &fb, const GemmArgs &g,
+                                          const Sched &sc, const Cursor<BN> &c, int tid) {
+    const StepSrc src = step_src(g, sc, c.it, c.s);
+    const int L = tc_unit_length(g.pad, src.unit, g.h, g.n);
+    frag_load<kTM>(fa, src.a, src.a.mat(src.unit, g.h), c.it.row0, src.k0, g.M, src.kend, L, tid);
+    frag_load<BN>(fb, src.b, src.b.mat(src.unit, g.h), c.it.col0, src.k0, g.N, src.kend, L, tid);
+}
+
+// Waits until ring stage step % stages is free, writes the step's split tiles into it
+// and marks it full.  False when a wait ran out (or another role gave up).
+template <int BN>
+__device__ __forceinline__ bool put_step(const Frag<kTM> &fa, const Frag<BN> &fb, int a_mn,
+                                         int b_mn, uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                         uint32_t &step, int *status, volatile int *abort_flag,
+                                         int tid) {
+    using C = Cfg<BN>;
+    const int s = (int)(step % C::kStages);
+    if (step >= (uint32_t)C::kStages &&
+        !warp_wait(empty + s, ((step / C::kStages) - 1) & 1, status, 32, abort_flag))
+        return false;
+    uint8_t *st = ring + s * C::kStage;
+    frag_store<kTM>(fa, a_mn, st, st + C::kA, tid);
+    frag_store<BN>(fb, b_mn, st + 2 * C::kA, st + 2 * C::kA + C::kB, tid);
+    fence_proxy_async_smem();
+    mbar_arrive(full + s);
+    ++step;
+    return true;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Eight 4-float groups of columns c .. c + 31 of one row (row pointer `row`, `cols`
+// columns): 16-byte loads when the row allows them, zero past the row's end.
+__device__ __forceinline__ void load_row32(float4 (&p)[8], const float *row, int c, int cols,
+                                           bool vec) {
+    if (vec && c + 32 <= cols) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) p[j] = __ldg(reinterpret_cast<const float4 *>(row + c + 4 * j));
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int q = c + 4 * j;
+        p[j].x = q < cols ? __ldg(row + q) : 0.f;
+        p[j].y = q + 1 < cols ? __ldg(row + q + 1) : 0.f;
+        p[j].z = q + 2 < cols ? __ldg(row + q + 2) : 0.f;
+        p[j].w = q + 3 < cols ? __ldg(row + q + 3) : 0.f;
+    }
+}
+__device__ __forceinline__ float pick(const float4 (&p)[8], int i) {
+    const float4 q = p[i >> 2];
+    return (i & 3) == 0 ? q.x : ((i & 3) == 1 ? q.y : ((i & 3) == 2 ? q.z : q.w));
+}
+
+// Epilogue of one tile by warp q (rows row0 + 32 q ..): the accumulator of TMEM columns
+// taddr .. taddr + BN, passed 32 columns at a time through the warp's transpose `tr`
+// (32 rows of kPitch floats: a lane's row, or a row's 32 columns, in 32 banks), so that
+// each store instruction writes 32 consecutive floats of one row.
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc, const Item &it,
+                                              uint32_t taddr, float *tr, int q, int lane) {
+    const int r0 = it.row0 + q * 32;
+    const bool acc = it.nk > 0;  // no product: the accumulator reads as zero
+    const bool rows_full = r0 + 32 <= g.M;
+    auto fetch = [&](int c, uint32_t (&v)[32]) {
+        if (acc) {
+            tmem_ld32(taddr + (uint32_t)c, v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+    };
+    // Rows r0 .. r0 + 31 of columns c0 + c .., from the transpose, to out (row stride ld).
+    auto store_rows = [&](float *out, int ld, int gc) {
+        if (gc >= g.N) return;
+        float *p = out + (long long)r0 * ld + gc;
+        if (rows_full) {
+#pragma unroll 8
+            for (int rr = 0; rr < 32; ++rr, p += ld) *p = tr[rr * kPitch + lane];
+        } else {
+            for (int rr = 0; rr < 32 && r0 + rr < g.M; ++rr, p += ld) *p = tr[rr * kPitch + lane];
+        }
+    };
+    if (g.epi == kEpiPlain) {
+        const int L = sc.usum ? g.n : tc_unit_length(g.pad, it.z, g.h, g.n);
+        const bool part = g.splits > 1;
+        float *out = part ? g.part + ((long long)it.split * sc.zcount + it.z) * g.M * g.N
+                          : g.C + (long long)it.z * g.sC;
+        const int ld = part ? g.N : g.ldc;
+        const bool simple = part || (g.beta == 0.f && !g.mask_rows && !g.mask_cols);
+        for (int c = 0; c < BN && it.col0 + c < g.N; c += 32) {
+            uint32_t v[32];
+            fetch(c, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) tr[lane * kPitch + i] = g.alpha * __uint_as_float(v[i]);
+            __syncwarp();
+            const int gc = it.col0 + c + lane;
+            if (simple) {
+                store_rows(out, ld, gc);
+            } else if (gc < g.N) {
+                float *p = out + (long long)r0 * ld + gc;
+                for (int rr = 0; rr < 32 && r0 + rr < g.M; ++rr, p += ld) {
+                    const int gr = r0 + rr;
+                    float val = tr[rr * kPitch + lane];
+                    if (g.beta != 0.f) val = fmaf(g.beta, *p, val);
+                    if ((g.mask_rows && gr >= L) || (g.mask_cols && gc >= L)) val = 0.f;
+                    *p = val;
+                }
+            }
+            __syncwarp();
+        }
+        return;
+    }
+    // Whole rows (col0 = 0, N <= BN): the lane's row is r0 + lane.
+    const int L = tc_unit_length(g.pad, it.z, g.h, g.n);
+    const bool live = r0 + lane < L;
+    float *out = g.C + (long long)it.z * g.sC;
+    const int N = g.N;
+    if (g.epi == kEpiSoftmax) {
+        // p = 2^(a2 s - m2) / l with a2 = alpha log2(e): one FFMA and one ex2 a value
+        const float a2 = g.alpha * kLog2e;
+        float m0 = -INFINITY, m1 = -INFINITY;
+        for (int c = 0; c < N; c += 32) {
+            uint32_t v[32];
+            fetch(c, v);
+            if (c + 32 <= N) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    m0 = fmaxf(m0, a2 * __uint_as_float(v[i]));
+                    m1 = fmaxf(m1, a2 * __uint_as_float(v[i + 1]));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c + i < N) m0 = fmaxf(m0, a2 * __uint_as_float(v[i]));
+            }
+        }
+        const float m = fmaxf(m0, m1);
+        float l0 = 0.f, l1 = 0.f;
+        for (int c = 0; c < N; c += 32) {
+            uint32_t v[32];
+            fetch(c, v);
+            if (c + 32 <= N) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    l0 += ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m));
+                    l1 += ex2_approx(fmaf(a2, __uint_as_float(v[i + 1]), -m));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c + i < N) l0 += ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m));
+            }
+        }
+        // rows at or past the length are exact zeros (their scores may be anything)
+        const float inv = 1.f / (l0 + l1);
+        for (int c = 0; c < N; c += 32) {
+            uint32_t v[32];
+            fetch(c, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                tr[lane * kPitch + i] = (live && c + i < N)
+                                            ? ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m)) * inv
+                                            : 0.f;
+            __syncwarp();
+            store_rows(out, g.ldc, c + lane);
+            __syncwarp();
+        }
+        return;
+    }
+    // kEpiSoftmaxBwd: dS = P (dP - D), dP = alpha * accumulator, D = sum_j P_j dP_j, with
+    // the lane reading its own row of P (whole 128-byte lines), the next 32 columns in
+    // flight while the current ones are used.
+    const bool row_ok = r0 + lane < g.M;
+    const float *prow = g.aux + (long long)it.z * g.sC + (long long)(row_ok ? r0 + lane : r0) * g.ldc;
+    const int pcols = row_ok ? N : 0;
+    const bool pvec = (g.ldc & 3) == 0 && ((reinterpret_cast<uintptr_t>(g.aux) & 15) == 0) &&
+                      ((g.sC & 3) == 0);
+    float4 pa[8], pb[8];
+    float D0 = 0.f, D1 = 0.f;
+    load_row32(pa, prow, 0, pcols, pvec);
+    for (int c = 0; c < N; c += 64) {
+        const bool second = c + 32 < N;
+        if (second) load_row32(pb, prow, c + 32, pcols, pvec);
+        uint32_t v[32];
+        fetch(c, v);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            D0 = fmaf(pick(pa, i), __uint_as_float(v[i]), D0);
+            D1 = fmaf(pick(pa, i + 1), __uint_as_float(v[i + 1]), D1);
+        }
+        if (!second) break;
+        if (c + 64 < N) load_row32(pa, prow, c + 64, pcols, pvec);
+        fetch(c + 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            D0 = fmaf(pick(pb, i), __uint_as_float(v[i]), D0);
+            D1 = fmaf(pick(pb, i + 1), __uint_as_float(v[i + 1]), D1);
+        }
+    }
+    const float D = g.alpha * (D0 + D1);
+    auto emit = [&](const float4 (&pp)[8], int c) {
+        uint32_t v[32];
+        fetch(c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            tr[lane * kPitch + i] = pick(pp, i) * fmaf(g.alpha, __uint_as_float(v[i]), -D);
+        __syncwarp();
+        store_rows(out, g.ldc, c + lane);
+        __syncwarp();
+    };
+    load_row32(pa, prow, 0, pcols, pvec);
+    for (int c = 0; c < N; c += 64) {
+        const bool second = c + 32 < N;
+        if (second) load_row32(pb, prow, c + 32, pcols, pvec);
+        emit(pa, c);
+        if (!second) break;
+        if (c + 64 < N) load_row32(pa, prow, c + 64, pcols, pvec);
+        emit(pb, c + 32);
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const GemmArgs g, const Sched sc) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *transpose = reinterpret_cast<float *>(ring + C::kRing);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + C::kRing + C::kTranspose);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *acc_full = empty + C::kStages;  // [2]
+    uint64_t *acc_empty = acc_full + 2;       // [2]
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full + s, kProducers);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int a_mn = g.A.xfast, b_mn = g.B.xfast;
+
+    if (warp < kProducerWarps) {
+        // ---- producers: global fp32 -> split bf16 hi / lo -> ring stage
+        uint32_t step = 0;
+        Cursor<BN> cur;
+        cur.start(g, sc);
+        Frag<kTM> fa0;
+        Frag<BN> fb0;
+        if constexpr (C::kPrefetch) {
+            Frag<kTM> fa1;
+            Frag<BN> fb1;
+            bool v0 = cur.valid(sc);
+            if (v0) load_step<BN>(fa0, fb0, g, sc, cur, tid);
+            while (v0) {
+                Cursor<BN> nx = cur;
+                nx.next(g, sc);
+                const bool v1 = nx.valid(sc);
+                if (v1) load_step<BN>(fa1, fb1, g, sc, nx, tid);
+                if (!put_step<BN>(fa0, fb0, a_mn, b_mn, ring, full, empty, step, g.status,
+                                  abort_flag, tid) || !v1)
+                    break;
+                cur = nx;
+                cur.next(g, sc);
+                v0 = cur.valid(sc);
+                if (v0) load_step<BN>(fa0, fb0, g, sc, cur, tid);
+                if (!put_step<BN>(fa1, fb1, a_mn, b_mn, ring, full, empty, step, g.status,
+                                  abort_flag, tid))
+                    break;
+            }
+        } else {
+            while (cur.valid(sc)) {
+                load_step<BN>(fa0, fb0, g, sc, cur, tid);
+                if (!put_step<BN>(fa0, fb0, a_mn, b_mn, ring, full, empty, step, g.status,
+                                  abort_flag, tid))
+                    break;
+                cur.next(g, sc);
+            }
+        }
+    } else if (warp < kMmaWarp) {
+        // ---- epilogue: TMEM accumulator -> C (or the split's partial)
+        const int q = warp & 3;
+        float *tr = transpose + q * 32 * kPitch;
+        int tcount = 0;
+        for (long long w = blockIdx.x; w < sc.items; w += gridDim.x, ++tcount) {
+            const Item it = item_at<BN>(g, sc, w);
+            const int b = tcount & 1;
+            if (!warp_wait(acc_full + b, (tcount >> 1) & 1, g.status, 33, abort_flag)) break;
+            tc_fence_after();
+            if (*abort_flag) break;
+            epilogue_tile<BN>(g, sc, it, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN), tr,
+                              q, lane);
+            tc_fence_before();
+            mbar_arrive(acc_empty + b);
+        }
+    } else if (lane == 0) {
+        // ---- MMA issuer
+        const uint32_t idesc = idesc_f16(kTM, BN, 1, a_mn, b_mn);
+        const uint64_t sa = slice_step(a_mn), sb = slice_step(b_mn);
+        uint32_t step = 0;
+        int tcount = 0;
+        bool ok = true;
+        for (long long w = blockIdx.x; ok && w < sc.items; w += gridDim.x, ++tcount) {
+            const Item it = item_at<BN>(g, sc, w);
+            const int b = tcount & 1;
+            if (tcount >= 2) ok = mbar_wait(acc_empty + b, ((tcount >> 1) - 1) & 1, g.status, 34,
+                                            abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(b * BN);
+            for (int s = 0; s < it.nk; ++s, ++step) {
+                const int st = (int)(step % C::kStages);
+                ok = mbar_wait(full + st, (step / C::kStages) & 1, g.status, 31, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t *base = ring + st * C::kStage;
+                const uint64_t ah = tile_desc(base, a_mn), al = tile_desc(base + C::kA, a_mn);
+                const uint64_t bh = tile_desc(base + 2 * C::kA, b_mn),
+                               bl = tile_desc(base + 2 * C::kA + C::kB, b_mn);
+#pragma unroll
+                for (int k = 0; k < kTK / 16; ++k) {
+                    mma_ss(d, ah + k * sa, bh + k * sb, idesc, (s > 0 || k > 0) ? 1u : 0u);
+                    mma_ss(d, ah + k * sa, bl + k * sb, idesc, 1u);
+                    mma_ss(d, al + k * sa, bh + k * sb, idesc, 1u);
+                }
+                mma_commit(empty + st);
+            }
+            if (!ok) break;
+            if (it.nk > 0) mma_commit(acc_full + b);
+            else mbar_arrive(acc_full + b);
+        }
+        // every product issued has finished before TMEM is released
+        mma_commit(drain);
+        mbar_wait_drain(drain, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int BN>
+int launch_tc_gemm(const GemmArgs &g, const Sched &sc, int sms, cudaStream_t s, int kernel_id) {
+    using C = Cfg<BN>;
+    static_assert(C::kSmem <= 227 * 1024, "shared memory of one CTA");
+    if (sc.items <= 0) return LINFORMER_OK;
+    const long long grid = std::min<long long>(sc.items, sms);
+    if (cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::kSmem) != cudaSuccess)
+        return LINFORMER_ERR_LAUNCH;
+    {
+        KernelScope scope(kernel_id, s);
+        tc_gemm_kernel<BN><<<(unsigned)grid, kThreads, C::kSmem, s>>>(g, sc);
+    }
+    if (cudaPeekAtLastError() != cudaSuccess) return LINFORMER_ERR_LAUNCH;
+    if (g.splits > 1) return launch_splitk_reduce(g, sc.zcount, s, kernel_id);
+    return LINFORMER_OK;
+}
+
+}  // namespace
+
+int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, size_t part_floats,
+                    int sms, int kernel_id) {
+    if (g.M <= 0 || g.N <= 0 || units <= 0) return LINFORMER_OK;
+    if (sms <= 0) sms = sm_count();
+    set_operand_vec(g.A, g.A.xfast ? g.M : g.K);
+    set_operand_vec(g.B, g.B.xfast ? g.N : g.K);
+    const bool usum = g.usum_groups > 0, two = usum && g.A2.p != nullptr;
+    if (two) {
+        if (g.A2.xfast != g.A.xfast || g.B2.xfast != g.B.xfast) return LINFORMER_ERR_SIZE;
+        set_operand_vec(g.A2, g.A2.xfast ? g.M : g.K);
+        set_operand_vec(g.B2, g.B2.xfast ? g.N : g.K);
+    }
+    const int BN = g.N <= 64 ? 64 : (g.N <= 128 ? 128 : 256);
+    if (g.epi != kEpiPlain && (g.N > BN || usum || (g.epi == kEpiSoftmaxBwd && !g.aux)))
+        return LINFORMER_ERR_SIZE;
+    Sched sc{};
+    sc.tiles_m = (g.M + kTM - 1) / kTM;
+    sc.tiles_n = (g.N + BN - 1) / BN;
+    sc.ksteps = (g.K + kTK - 1) / kTK;
+    sc.usum = usum ? 1 : 0;
+    sc.zcount = usum ? g.usum_groups : units;
+    sc.terms = two ? 2 : 1;
+    sc.per_group = g.usum_per_group;
+    sc.ga = g.usum_ga;
+    sc.gb = g.usum_gb;
+    g.splits = 1;
+    g.kchunk = sc.ksteps * kTK;
+    g.part = part;
+    g.status = device_status_ptr();
+    const long long tiles = (long long)sc.tiles_m * sc.tiles_n * sc.zcount;
+    const long long out_floats = (long long)sc.zcount * g.M * g.N;
+    // Splits (or unit chunks) for about four work items per SM, as far as the partials
+    // fit in `part`; a split is at least four steps deep.
+    long long want = 1;
+    if (g.epi == kEpiPlain && part && tiles < 4LL * sms) {
+        want = (4LL * sms + tiles - 1) / tiles;
+        want = std::min<long long>(want, (long long)(part_floats / (size_t)out_floats));
+        if (usum)
+            want = std::min<long long>(want, sc.per_group);
+        else
+            want = std::min<long long>(want, std::max(1, sc.ksteps / 4));
+        want = std::max<long long>(want, 1);
+    }
+    if (usum) {
+        sc.uc = (int)((sc.per_group + want - 1) / want);
+        g.splits = sc.uc > 0 ? (sc.per_group + sc.uc - 1) / sc.uc : 1;
+    } else if (want > 1) {
+        const int steps = (int)((sc.ksteps + want - 1) / want);
+        g.kchunk = steps * kTK;
+        g.splits = (sc.ksteps + steps - 1) / steps;
+    }
+    sc.splits = g.splits;
+    sc.items = tiles * sc.splits;
+    if (BN == 64) return launch_tc_gemm<64>(g, sc, sms, s, kernel_id);
+    if (BN == 128) return launch_tc_gemm<128>(g, sc, sms, s, kernel_id);
+    return launch_tc_gemm<256>(g, sc, sms, s, kernel_id);
+}
+
+}  // namespace simt
+}  // namespace linformer

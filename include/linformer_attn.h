@@ -188,9 +188,9 @@ LINFORMER_API int linformer_attn_fwd_noalloc(const void *Q, const void *K, const
  * it.  fp32 only (LINFORMER_F32; other dtypes return LINFORMER_ERR_UNSUPPORTED),
  * d <= 128, k <= 1024, b*h <= 65535 (else LINFORMER_ERR_SIZE).  All pointers are
  * device pointers, 16-byte aligned; the caller owns every buffer; a stream-ordered
- * workspace of b*h*(2 n k + k n + 12 k d) floats (plus b*h*k*n with a distinct F;
- * 8 k d of the 12 hold split partial sums) comes from the library's pool and is
- * returned to it in stream order.
+ * workspace of b*h*(2 n k + 12 k d) floats (8 k d of the 12 hold split partial sums;
+ * the 2 n k, once P and dS are used, the partial sums of dE and dF) comes from the
+ * library's pool and is returned to it in stream order.
  */
 LINFORMER_API int linformer_attn_bwd(const void *Q, const void *K, const void *V,
                                      const void *E, const void *F, const int32_t *pad_lengths,

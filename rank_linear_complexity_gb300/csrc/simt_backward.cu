@@ -100,13 +100,27 @@ int simt_backward(const Problem &p, const float *dO, float *dQ, float *dK, float
     if (!st) st = tc_batched_gemm(args(opA(dS, nk, k, 1, kPerUnit), opB(Q, nd, d, 0, kPerUnit, 1), dKb,
                                        kd, d, k, d, n, scale, 0.f, 0, 0),
                                   units, s, part, part_floats, sms);
-    // dK = E^T dKbar, dV = F^T dVbar (rows >= L zero)
-    if (!st) st = tc_batched_gemm(args(opA(E, kn, n, 1, pidx), opB(dKb, kd, d, 0, kPerUnit), dK, nd, d,
-                                       n, d, k, 1.f, 0.f, 1, 0),
-                                  units, s, nullptr, 0, sms);
-    if (!st) st = tc_batched_gemm(args(opA(F, kn, n, 1, pidx), opB(dVb, kd, d, 0, kPerUnit), dV, nd, d,
-                                       n, d, k, 1.f, 0.f, 1, 0),
-                                  units, s, nullptr, 0, sms);
+    // dK = E^T dKbar, dV = F^T dVbar (rows >= L zero); with d a multiple of 32 the units
+    // sharing E (F) side by side along N
+    auto project_back = [&](const float *X, const float *dXb, float *dX) {
+        GemmArgs g = args(opA(X, kn, n, 1, pidx), opB(dXb, kd, d, 0, kPerUnit), dX, nd, d, n, d, k,
+                          1.f, 0.f, 1, 0);
+        int zcount = units;
+        if (d % 32 == 0) {
+            const int groups = per_head ? h : 1, ub = per_head ? h : 1;
+            zcount = groups;
+            g.N = (units / groups) * d;
+            g.B.xblk = d;
+            g.B.blk_stride = ub * kd;
+            g.cblk = d;
+            g.cblk_stride = ub * nd;
+            g.blk_ua = per_head ? 1 : 0;
+            g.blk_ub = ub;
+        }
+        return tc_batched_gemm(g, zcount, s, nullptr, 0, sms);
+    };
+    if (!st) st = project_back(E, dKb, dK);
+    if (!st) st = project_back(F, dVb, dV);
     // dE (and dF) = the sum over the units sharing the matrix of dKbar K^T (dVbar V^T),
     // columns t >= L of each unit's term zero; P and dS, no longer needed, hold the
     // partial sums.

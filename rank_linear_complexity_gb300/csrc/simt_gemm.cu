@@ -173,12 +173,15 @@ __global__ void splitk_reduce_kernel(const GemmArgs g, long long units) {
     const int z = (int)(i / mn);
     const long long e = i % mn;
     const int r = (int)(e / g.N), c = (int)(e % g.N);
-    const int L = unit_length(g.pad, z, g.h, g.n);
+    // column blocks (tensor-core product): block c / cblk of unit z blk_ua + block blk_ub
+    const int blk = g.cblk > 0 ? c / g.cblk : 0, cc = g.cblk > 0 ? c % g.cblk : c;
+    const int unit = g.cblk > 0 ? z * g.blk_ua + blk * g.blk_ub : z;
+    const int L = unit_length(g.pad, unit, g.h, g.n);
     float v = 0.f;
     for (int sp = 0; sp < g.splits; ++sp) v += g.part[((long long)sp * units + z) * mn + e];
-    float *C = g.C + (long long)z * g.sC + (long long)r * g.ldc + c;
+    float *C = g.C + (long long)z * g.sC + blk * g.cblk_stride + (long long)r * g.ldc + cc;
     if (g.beta != 0.f) v = fmaf(g.beta, *C, v);
-    if ((g.mask_rows && r >= L) || (g.mask_cols && c >= L)) v = 0.f;
+    if ((g.mask_rows && r >= L) || (g.mask_cols && cc >= L)) v = 0.f;
     *C = v;
 }
 
@@ -298,21 +301,38 @@ int project_f32(const Problem &p, float *Kbar, float *Vbar, float *part, int ker
                 bool tensor) {
     const int units = (int)p.units(), n = p.n, d = p.d, k = p.k;
     const long long kd = (long long)k * d, nd = (long long)n * d, kn = (long long)k * n;
-    const int pidx = p.proj_per_head() ? kPerHead : kShared;
+    const bool per_head = p.proj_per_head();
+    const int pidx = per_head ? kPerHead : kShared;
     const int sms = sm_count();
     const float *K = static_cast<const float *>(p.K), *V = static_cast<const float *>(p.V);
     const float *E = static_cast<const float *>(p.E), *F = static_cast<const float *>(p.f_or_e());
     GemmArgs g{opA(E, kn, n, 0, pidx), opB(K, nd, d, 0, kPerUnit, 1), Kbar, kd, d, k, d, n, 1.f,
                0.f, p.pad, p.h, n, 0, 0, 1, 0, nullptr};
+    int zcount = units;
+    if (tensor && d % 32 == 0) {
+        // the units sharing E side by side along N: E's tiles feed several units at once
+        const int groups = per_head ? p.h : 1, ub = per_head ? p.h : 1;
+        zcount = groups;
+        g.N = (units / groups) * d;
+        g.B.xblk = d;
+        g.B.blk_stride = ub * nd;
+        g.cblk = d;
+        g.cblk_stride = ub * kd;
+        g.blk_ua = per_head ? 1 : 0;
+        g.blk_ub = ub;
+    }
     auto product = [&](const GemmArgs &a) {
-        return tensor ? tc_batched_gemm(a, units, p.stream, part,
+        return tensor ? tc_batched_gemm(a, zcount, p.stream, part,
                                         (size_t)kMaxSplits * units * kd, sms, kernel_id)
                       : batched_gemm(a, units, p.stream, part, kMaxSplits, sms, kernel_id);
     };
     int st = product(g);
     if (st) return st;
     g.A = opA(F, kn, n, 0, pidx);
+    const Operand b = g.B;
     g.B = opB(V, nd, d, 0, kPerUnit, 1);
+    g.B.xblk = b.xblk;
+    g.B.blk_stride = b.blk_stride;
     g.C = Vbar;
     return product(g);
 }

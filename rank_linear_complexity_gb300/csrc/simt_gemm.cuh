@@ -23,6 +23,11 @@ struct Operand {
     int mask_x, mask_k;  // 1: x (resp. kk) >= the unit's length reads as zero (the
                          // sequence axis of Q, K, V, dO: padded rows may hold anything)
     int vec;           // 1: 4-element groups along the contiguous axis are 16-byte loads
+    // Tensor-core product only, x contiguous: x splits into blocks of xblk (a multiple of
+    // 32; 0: none), block j of matrix z at mat(z) + j blk_stride, so that one product
+    // covers the units that share the other operand side by side along N.
+    int xblk = 0;
+    long long blk_stride = 0;
     __device__ __forceinline__ const float *mat(int z, int h) const {
         const int m = index == kPerUnit ? z : (index == kPerHead ? z % h : 0);
         return p + (long long)m * stride;
@@ -53,6 +58,12 @@ struct GemmArgs {
     // output masks must be off.
     int usum_groups = 0, usum_per_group = 0, usum_ga = 0, usum_gb = 0;
     Operand A2{}, B2{};
+    // cblk > 0 (with B.xblk == cblk): C's columns in blocks of cblk, block j of output
+    // matrix z at C + z sC + j cblk_stride; block j of matrix z belongs to unit
+    // z blk_ua + j blk_ub (its length masks B's sequence axis and C's rows).
+    int cblk = 0;
+    long long cblk_stride = 0;
+    int blk_ua = 0, blk_ub = 0;
 };
 
 // What the tensor-core product writes: alpha A B (+ beta C, output masks), the row

@@ -52,7 +52,7 @@ constexpr int kProducers = kProducerWarps * 32;
 constexpr int kEpilogueWarp0 = kProducerWarps;  // warps 8..11: lane quarters 0..3
 constexpr int kMmaWarp = kProducerWarps + 4;     // warp 12
 constexpr int kThreads = (kMmaWarp + 1) * 32;    // 416
-constexpr int kPitch = 33;                       // floats per row of a warp's transpose
+constexpr int kStagePitch = 36;                  // floats per lane's staging row (144 B)
 static_assert(kEpilogueWarp0 % 4 == 0, "epilogue warp w reads TMEM lanes 32 (w % 4) ..");
 
 // Stages of the ring (192 KB of operand tiles for every BN) and the shared memory in all.
@@ -62,10 +62,9 @@ struct Cfg {
     static constexpr uint32_t kA = kTM * kTK * 2, kB = BN * kTK * 2;  // one hi (or lo) tile
     static constexpr uint32_t kStage = 2 * kA + 2 * kB;
     static constexpr uint32_t kRing = kStages * kStage;
-    static constexpr uint32_t kTranspose = 4 * 32 * kPitch * 4;
+    static constexpr uint32_t kTranspose = 4 * 32 * kStagePitch * 4;  // staging rows
     static constexpr uint32_t kTmemCols = 2 * BN;  // 128, 256 or 512: a power of two
     static constexpr size_t kSmem = 1024 + kRing + kTranspose + 256;
-    static constexpr bool kPrefetch = false;      // two steps of loads in flight
 };
 
 __device__ __forceinline__ int tc_unit_length(const int32_t *pad, int unit, int h, int n) {
@@ -158,32 +157,38 @@ __device__ __forceinline__ void frag_load(Frag<BX> &f, const Operand &o, const f
     }
 }
 
-// Splits the loaded groups and writes hi and lo into their tiles.  The swizzle phase
-// of a group's row (row % 8) is the same for all of a thread's groups except along x
-// with BX = 256, where it alternates.
+// The hi and lo parts of a thread's groups.
 template <int BX>
-__device__ __forceinline__ void frag_store(const Frag<BX> &f, int xfast, uint8_t *hi, uint8_t *lo,
-                                           int tid) {
+struct Split {
+    uint2 h[Frag<BX>::kGroups], l[Frag<BX>::kGroups];
+};
+template <int BX>
+__device__ __forceinline__ void split_frag(const Frag<BX> &f, Split<BX> &sp) {
+#pragma unroll
+    for (int g = 0; g < Frag<BX>::kGroups; ++g) split4(f.v[g], sp.h[g], sp.l[g]);
+}
+// Writes the split groups into their hi and lo tiles.  The swizzle phase of a group's
+// row (row % 8) is the same for all of a thread's groups except along x with BX = 256,
+// where it alternates.
+template <int BX>
+__device__ __forceinline__ void store_split(const Split<BX> &sp, int xfast, uint8_t *hi, uint8_t *lo,
+                                            int tid) {
     using F = Frag<BX>;
     if (xfast) {
         const int xr = (tid % F::kRowThreads) * 4, kr0 = tid / F::kRowThreads;
 #pragma unroll
         for (int g = 0; g < F::kGroups; ++g) {
-            uint2 h, l;
-            split4(f.v[g], h, l);
             const uint32_t off = mnmajor_off(xr, kr0 + g * F::kKRowsPerGroup);
-            *reinterpret_cast<uint2 *>(hi + off) = h;
-            *reinterpret_cast<uint2 *>(lo + off) = l;
+            *reinterpret_cast<uint2 *>(hi + off) = sp.h[g];
+            *reinterpret_cast<uint2 *>(lo + off) = sp.l[g];
         }
     } else {
         const uint32_t off0 = kmajor_off(tid / 16, (tid % 16) * 4);
 #pragma unroll
         for (int g = 0; g < F::kGroups; ++g) {
-            uint2 h, l;
-            split4(f.v[g], h, l);
             const uint32_t off = off0 + (uint32_t)g * 16u * 128u;  // 16 rows on, same phase
-            *reinterpret_cast<uint2 *>(hi + off) = h;
-            *reinterpret_cast<uint2 *>(lo + off) = l;
+            *reinterpret_cast<uint2 *>(hi + off) = sp.h[g];
+            *reinterpret_cast<uint2 *>(lo + off) = sp.l[g];
         }
     }
 }
@@ -298,11 +303,21 @@ __device__ __forceinline__ void load_step(Frag<kTM> &fa, Frag<BN> &fb, const Gem
     const StepSrc src = step_src(g, sc, c.it, c.s);
     const int L = tc_unit_length(g.pad, src.unit, g.h, g.n);
     frag_load<kTM>(fa, src.a, src.a.mat(src.unit, g.h), c.it.row0, src.k0, g.M, src.kend, L, tid);
-    frag_load<BN>(fb, src.b, src.b.mat(src.unit, g.h), c.it.col0, src.k0, g.N, src.kend, L, tid);
+    const float *mb = src.b.mat(src.unit, g.h);
+    int Lb = L;
+    if (src.b.xblk) {
+        // the thread's columns lie in one block (x is fixed across its groups): its unit's
+        // matrix and length; mb is offset so that mb + k ld + x addresses column x
+        const int x = min(c.it.col0 + (tid % Frag<BN>::kRowThreads) * 4, g.N - 1);
+        const int blk = x / src.b.xblk;
+        mb += blk * src.b.blk_stride - (long long)blk * src.b.xblk;
+        Lb = tc_unit_length(g.pad, c.it.z * g.blk_ua + blk * g.blk_ub, g.h, g.n);
+    }
+    frag_load<BN>(fb, src.b, mb, c.it.col0, src.k0, g.N, src.kend, Lb, tid);
 }
-
 // Waits until ring stage step % stages is free, writes the step's split tiles into it
 // and marks it full.  False when a wait ran out (or another role gave up).
+// The loads stay in flight during the wait; the split follows it.
 template <int BN>
 __device__ __forceinline__ bool put_step(const Frag<kTM> &fa, const Frag<BN> &fb, int a_mn,
                                          int b_mn, uint8_t *ring, uint64_t *full, uint64_t *empty,
@@ -313,11 +328,16 @@ __device__ __forceinline__ bool put_step(const Frag<kTM> &fa, const Frag<BN> &fb
     if (step >= (uint32_t)C::kStages &&
         !warp_wait(empty + s, ((step / C::kStages) - 1) & 1, status, 32, abort_flag))
         return false;
+    Split<kTM> sa;
+    Split<BN> sb;
+    split_frag<kTM>(fa, sa);
+    split_frag<BN>(fb, sb);
     uint8_t *st = ring + s * C::kStage;
-    frag_store<kTM>(fa, a_mn, st, st + C::kA, tid);
-    frag_store<BN>(fb, b_mn, st + 2 * C::kA, st + 2 * C::kA + C::kB, tid);
+    store_split<kTM>(sa, a_mn, st, st + C::kA, tid);
+    store_split<BN>(sb, b_mn, st + 2 * C::kA, st + 2 * C::kA + C::kB, tid);
     fence_proxy_async_smem();
-    mbar_arrive(full + s);
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(full + s);  // one arrival per producer warp
     ++step;
     return true;
 }
@@ -347,16 +367,49 @@ __device__ __forceinline__ float pick(const float4 (&p)[8], int i) {
     return (i & 3) == 0 ? q.x : ((i & 3) == 1 ? q.y : ((i & 3) == 2 ? q.z : q.w));
 }
 
-// Epilogue of one tile by warp q (rows row0 + 32 q ..): the accumulator of TMEM columns
-// taddr .. taddr + BN, passed 32 columns at a time through the warp's transpose `tr`
-// (32 rows of kPitch floats: a lane's row, or a row's 32 columns, in 32 banks), so that
-// each store instruction writes 32 consecutive floats of one row.
+// The warp's output of one 32-column chunk of rows r0 .. r0 + 31 (lane l holds row
+// r0 + l in val): each lane writes its row into the warp's staging rows (kStagePitch
+// floats apart: a quarter-warp's 16-byte stores or loads fall in distinct banks), then
+// each store instruction writes four whole 128-byte row pieces, eight lanes a row.
+// chunk points at row 0 of the chunk's first column (row stride ld); rows >= M and
+// columns >= ncols are not written; `vec`: 16-byte stores (16-byte-aligned rows).
+__device__ __forceinline__ void emit_rows32(const float (&val)[32], float *chunk, long long ld,
+                                            int r0, int ncols, int M, float *stg, int lane,
+                                            bool vec) {
+    float4 *mine = reinterpret_cast<float4 *>(stg + lane * kStagePitch);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        mine[j] = make_float4(val[4 * j], val[4 * j + 1], val[4 * j + 2], val[4 * j + 3]);
+    __syncwarp();
+    const int cc = (lane & 7) * 4;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const int rr = 4 * t + (lane >> 3), gr = r0 + rr;
+        const float4 x = reinterpret_cast<const float4 *>(stg + rr * kStagePitch)[lane & 7];
+        if (gr < M && cc < ncols) {
+            float *dst = chunk + (long long)gr * ld + cc;
+            if (vec && cc + 4 <= ncols) {
+                *reinterpret_cast<float4 *>(dst) = x;
+            } else {
+                dst[0] = x.x;
+                if (cc + 1 < ncols) dst[1] = x.y;
+                if (cc + 2 < ncols) dst[2] = x.z;
+                if (cc + 3 < ncols) dst[3] = x.w;
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// Epilogue of one tile by warp q: lane l owns row r0 + l (r0 = row0 + 32 q, TMEM lane
+// 32 q + l) and reads the accumulator of TMEM columns taddr .., 32 at a time; stg is
+// the warp's 32 staging rows.
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc, const Item &it,
-                                              uint32_t taddr, float *tr, int q, int lane) {
-    const int r0 = it.row0 + q * 32;
+                                              uint32_t taddr, float *stg, int q, int lane) {
+    const int r0 = it.row0 + q * 32, row = r0 + lane;
     const bool acc = it.nk > 0;  // no product: the accumulator reads as zero
-    const bool rows_full = r0 + 32 <= g.M;
+    const bool row_ok = row < g.M;
     auto fetch = [&](int c, uint32_t (&v)[32]) {
         if (acc) {
             tmem_ld32(taddr + (uint32_t)c, v);
@@ -365,109 +418,98 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc
             for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
     };
-    // Rows r0 .. r0 + 31 of columns c0 + c .., from the transpose, to out (row stride ld).
-    auto store_rows = [&](float *out, int ld, int gc) {
-        if (gc >= g.N) return;
-        float *p = out + (long long)r0 * ld + gc;
-        if (rows_full) {
-#pragma unroll 8
-            for (int rr = 0; rr < 32; ++rr, p += ld) *p = tr[rr * kPitch + lane];
-        } else {
-            for (int rr = 0; rr < 32 && r0 + rr < g.M; ++rr, p += ld) *p = tr[rr * kPitch + lane];
-        }
-    };
     if (g.epi == kEpiPlain) {
         const int L = sc.usum ? g.n : tc_unit_length(g.pad, it.z, g.h, g.n);
         const bool part = g.splits > 1;
+        const bool blocks = !part && g.cblk > 0;
         float *out = part ? g.part + ((long long)it.split * sc.zcount + it.z) * g.M * g.N
                           : g.C + (long long)it.z * g.sC;
         const int ld = part ? g.N : g.ldc;
-        const bool simple = part || (g.beta == 0.f && !g.mask_rows && !g.mask_cols);
+        const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0 && (ld & 3) == 0 &&
+                         (!blocks || (g.cblk_stride & 3) == 0);
+        const bool beta = !part && g.beta != 0.f;
         for (int c = 0; c < BN && it.col0 + c < g.N; c += 32) {
             uint32_t v[32];
             fetch(c, v);
+            const int gc = it.col0 + c;
+            // the chunk's place in C, its first column within its block and its length
+            float *chunk = out + gc;
+            int cb = gc, Lc = L;
+            if (blocks) {
+                const int blk = gc / g.cblk;
+                cb = gc - blk * g.cblk;
+                chunk = out + blk * g.cblk_stride + cb;
+                Lc = tc_unit_length(g.pad, it.z * g.blk_ua + blk * g.blk_ub, g.h, g.n);
+            }
+            float val[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) tr[lane * kPitch + i] = g.alpha * __uint_as_float(v[i]);
-            __syncwarp();
-            const int gc = it.col0 + c + lane;
-            if (simple) {
-                store_rows(out, ld, gc);
-            } else if (gc < g.N) {
-                float *p = out + (long long)r0 * ld + gc;
-                for (int rr = 0; rr < 32 && r0 + rr < g.M; ++rr, p += ld) {
-                    const int gr = r0 + rr;
-                    float val = tr[rr * kPitch + lane];
-                    if (g.beta != 0.f) val = fmaf(g.beta, *p, val);
-                    if ((g.mask_rows && gr >= L) || (g.mask_cols && gc >= L)) val = 0.f;
-                    *p = val;
+            for (int i = 0; i < 32; ++i) val[i] = g.alpha * __uint_as_float(v[i]);
+            if (beta && row_ok) {
+                const float *cr = chunk + (long long)row * ld;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (gc + i < g.N) val[i] = fmaf(g.beta, cr[i], val[i]);
+            }
+            if (!part) {
+                const bool zero_row = g.mask_rows && row >= Lc;
+                if (zero_row || g.mask_cols) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (zero_row || (g.mask_cols && cb + i >= Lc)) val[i] = 0.f;
                 }
             }
-            __syncwarp();
+            emit_rows32(val, chunk, ld, r0, min(32, g.N - gc), g.M, stg, lane, vec);
         }
         return;
     }
-    // Whole rows (col0 = 0, N <= BN): the lane's row is r0 + lane.
+    // Whole rows (col0 = 0, N <= BN).
     const int L = tc_unit_length(g.pad, it.z, g.h, g.n);
-    const bool live = r0 + lane < L;
-    float *out = g.C + (long long)it.z * g.sC;
+    const bool live = row < L;
     const int N = g.N;
+    float *out = g.C + (long long)it.z * g.sC;
+    const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0 && (g.ldc & 3) == 0;
     if (g.epi == kEpiSoftmax) {
-        // p = 2^(a2 s - m2) / l with a2 = alpha log2(e): one FFMA and one ex2 a value
+        // p = 2^(a2 s - m) / l with a2 = alpha log2(e); m and l in one pass (the running
+        // sum rescaled when the running maximum grows), p in a second
         const float a2 = g.alpha * kLog2e;
-        float m0 = -INFINITY, m1 = -INFINITY;
+        float m = -INFINITY, l = 0.f;
         for (int c = 0; c < N; c += 32) {
             uint32_t v[32];
             fetch(c, v);
-            if (c + 32 <= N) {
+            float cm0 = -INFINITY, cm1 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    m0 = fmaxf(m0, a2 * __uint_as_float(v[i]));
-                    m1 = fmaxf(m1, a2 * __uint_as_float(v[i + 1]));
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (c + i < N) m0 = fmaxf(m0, a2 * __uint_as_float(v[i]));
+            for (int i = 0; i < 32; i += 2) {
+                if (c + i < N) cm0 = fmaxf(cm0, a2 * __uint_as_float(v[i]));
+                if (c + i + 1 < N) cm1 = fmaxf(cm1, a2 * __uint_as_float(v[i + 1]));
             }
-        }
-        const float m = fmaxf(m0, m1);
-        float l0 = 0.f, l1 = 0.f;
-        for (int c = 0; c < N; c += 32) {
-            uint32_t v[32];
-            fetch(c, v);
-            if (c + 32 <= N) {
+            const float mn = fmaxf(m, fmaxf(cm0, cm1));
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    l0 += ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m));
-                    l1 += ex2_approx(fmaf(a2, __uint_as_float(v[i + 1]), -m));
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (c + i < N) l0 += ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m));
+            for (int i = 0; i < 32; i += 2) {
+                if (c + i < N) s0 += ex2_approx(fmaf(a2, __uint_as_float(v[i]), -mn));
+                if (c + i + 1 < N) s1 += ex2_approx(fmaf(a2, __uint_as_float(v[i + 1]), -mn));
             }
+            l = fmaf(l, ex2_approx(m - mn), s0 + s1);
+            m = mn;
         }
         // rows at or past the length are exact zeros (their scores may be anything)
-        const float inv = 1.f / (l0 + l1);
+        const float inv = 1.f / l;
         for (int c = 0; c < N; c += 32) {
             uint32_t v[32];
             fetch(c, v);
+            float val[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-                tr[lane * kPitch + i] = (live && c + i < N)
-                                            ? ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m)) * inv
-                                            : 0.f;
-            __syncwarp();
-            store_rows(out, g.ldc, c + lane);
-            __syncwarp();
+                val[i] = (live && c + i < N) ? ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m)) * inv
+                                             : 0.f;
+            emit_rows32(val, out + c, g.ldc, r0, min(32, N - c), g.M, stg, lane, vec);
         }
         return;
     }
     // kEpiSoftmaxBwd: dS = P (dP - D), dP = alpha * accumulator, D = sum_j P_j dP_j, with
     // the lane reading its own row of P (whole 128-byte lines), the next 32 columns in
     // flight while the current ones are used.
-    const bool row_ok = r0 + lane < g.M;
-    const float *prow = g.aux + (long long)it.z * g.sC + (long long)(row_ok ? r0 + lane : r0) * g.ldc;
+    const float *prow = g.aux + (long long)it.z * g.sC + (long long)(row_ok ? row : r0) * g.ldc;
     const int pcols = row_ok ? N : 0;
     const bool pvec = (g.ldc & 3) == 0 && ((reinterpret_cast<uintptr_t>(g.aux) & 15) == 0) &&
                       ((g.sC & 3) == 0);
@@ -497,12 +539,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc
     auto emit = [&](const float4 (&pp)[8], int c) {
         uint32_t v[32];
         fetch(c, v);
+        float val[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            tr[lane * kPitch + i] = pick(pp, i) * fmaf(g.alpha, __uint_as_float(v[i]), -D);
-        __syncwarp();
-        store_rows(out, g.ldc, c + lane);
-        __syncwarp();
+        for (int i = 0; i < 32; ++i) val[i] = pick(pp, i) * fmaf(g.alpha, __uint_as_float(v[i]), -D);
+        emit_rows32(val, out + c, g.ldc, r0, min(32, N - c), g.M, stg, lane, vec);
     };
     load_row32(pa, prow, 0, pcols, pvec);
     for (int c = 0; c < N; c += 64) {
@@ -532,12 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const GemmArgs g, 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(full + s, kProducers);
+            mbar_init(full + s, kProducerWarps);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, 128);
+            mbar_init(acc_empty + b, 4);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -558,42 +598,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const GemmArgs g, 
         uint32_t step = 0;
         Cursor<BN> cur;
         cur.start(g, sc);
-        Frag<kTM> fa0;
-        Frag<BN> fb0;
-        if constexpr (C::kPrefetch) {
-            Frag<kTM> fa1;
-            Frag<BN> fb1;
-            bool v0 = cur.valid(sc);
-            if (v0) load_step<BN>(fa0, fb0, g, sc, cur, tid);
-            while (v0) {
-                Cursor<BN> nx = cur;
-                nx.next(g, sc);
-                const bool v1 = nx.valid(sc);
-                if (v1) load_step<BN>(fa1, fb1, g, sc, nx, tid);
-                if (!put_step<BN>(fa0, fb0, a_mn, b_mn, ring, full, empty, step, g.status,
-                                  abort_flag, tid) || !v1)
-                    break;
-                cur = nx;
-                cur.next(g, sc);
-                v0 = cur.valid(sc);
-                if (v0) load_step<BN>(fa0, fb0, g, sc, cur, tid);
-                if (!put_step<BN>(fa1, fb1, a_mn, b_mn, ring, full, empty, step, g.status,
-                                  abort_flag, tid))
-                    break;
-            }
-        } else {
-            while (cur.valid(sc)) {
-                load_step<BN>(fa0, fb0, g, sc, cur, tid);
-                if (!put_step<BN>(fa0, fb0, a_mn, b_mn, ring, full, empty, step, g.status,
-                                  abort_flag, tid))
-                    break;
-                cur.next(g, sc);
-            }
+        while (cur.valid(sc)) {
+            Frag<kTM> fa;
+            Frag<BN> fb;
+            load_step<BN>(fa, fb, g, sc, cur, tid);
+            if (!put_step<BN>(fa, fb, a_mn, b_mn, ring, full, empty, step, g.status, abort_flag, tid))
+                break;
+            cur.next(g, sc);
         }
     } else if (warp < kMmaWarp) {
         // ---- epilogue: TMEM accumulator -> C (or the split's partial)
         const int q = warp & 3;
-        float *tr = transpose + q * 32 * kPitch;
+        float *stg = transpose + q * 32 * kStagePitch;
         int tcount = 0;
         for (long long w = blockIdx.x; w < sc.items; w += gridDim.x, ++tcount) {
             const Item it = item_at<BN>(g, sc, w);
@@ -601,10 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const GemmArgs g, 
             if (!warp_wait(acc_full + b, (tcount >> 1) & 1, g.status, 33, abort_flag)) break;
             tc_fence_after();
             if (*abort_flag) break;
-            epilogue_tile<BN>(g, sc, it, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN), tr,
+            epilogue_tile<BN>(g, sc, it, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN), stg,
                               q, lane);
             tc_fence_before();
-            mbar_arrive(acc_empty + b);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + b);  // one arrival per epilogue warp
         }
     } else if (lane == 0) {
         // ---- MMA issuer
@@ -683,6 +700,14 @@ int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, size_t p
         if (g.A2.xfast != g.A.xfast || g.B2.xfast != g.B.xfast) return LINFORMER_ERR_SIZE;
         set_operand_vec(g.A2, g.A2.xfast ? g.M : g.K);
         set_operand_vec(g.B2, g.B2.xfast ? g.N : g.K);
+    }
+    if (g.B.xblk || g.cblk || g.A.xblk) {
+        // column blocks: B x-contiguous in blocks of a multiple of 32 columns, C blocked
+        // alike, the length masks only on B's sequence axis and C's rows
+        if (g.A.xblk || !g.B.xfast || g.B.xblk <= 0 || g.B.xblk % 32 || g.cblk != g.B.xblk ||
+            g.B.mask_x || g.A.mask_x || g.A.mask_k || g.mask_cols || usum || g.epi != kEpiPlain)
+            return LINFORMER_ERR_SIZE;
+        if (g.B.blk_stride & 3) g.B.vec = 0;
     }
     const int BN = g.N <= 64 ? 64 : (g.N <= 128 ? 128 : 256);
     if (g.epi != kEpiPlain && (g.N > BN || usum || (g.epi == kEpiSoftmaxBwd && !g.aux)))

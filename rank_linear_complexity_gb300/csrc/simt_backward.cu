@@ -14,9 +14,10 @@
 // Every product, Kbar and Vbar included, runs on the batched tensor-core product of
 // tc_gemm.cu (fp32 operands split into bf16 hi + lo, three products, fp32 accumulation):
 // split over the sequence for the four k x d results that sum over it; with k <= 256
-// the softmax and the softmax backward in the epilogues of the products that make S and
-// dP (else the row softmax of simt_gemm.cu and the row kernel here); dE and dF as sums
-// over units inside the product, in chunks of units whose partials are then added.
+// S and dP of a row tile as one work item whose epilogue writes P and dS (else the row
+// softmax of simt_gemm.cu and the row kernel here); Kbar, Vbar, dK and dV with the
+// units sharing E or F side by side; dE and dF as sums over units inside the product,
+// in chunks of units whose partials are then added.
 #include "simt_gemm.cuh"
 
 namespace linformer {
@@ -70,25 +71,30 @@ int simt_backward(const Problem &p, const float *dO, float *dQ, float *dK, float
     const bool fused = k <= 256;
     // Kbar = E K, Vbar = F V over rows t < L
     int st = project_f32(p, Kb, Vb, part, LINFORMER_KERNEL_BACKWARD, true);
-    // P = softmax(Q Kbar^T / sqrt(d)) (rows >= L zero)
+    // P = softmax(Q Kbar^T / sqrt(d)) (rows >= L zero); dP = dO Vbar^T and
+    // dS = P * (dP - rowsum(P * dP)): with k <= 256 both products of a row tile in one
+    // work item, P and dS formed together in its epilogue
     GemmArgs gs = args(opA(Q, nd, d, 0, kPerUnit), opB(Kb, kd, d, 1, kPerUnit), P, nk, k, n, k, d,
                        scale, 0.f, 0, 0);
-    if (fused) gs.epi = kEpiSoftmax;
-    if (!st) st = tc_batched_gemm(gs, units, s, nullptr, 0, sms);
-    if (!st && !fused) st = softmax_rows(P, p.pad, h, n, k, units, 0, s);
-    // dP = dO Vbar^T, dS = P * (dP - rowsum(P * dP))
-    GemmArgs gp = args(opA(dO, nd, d, 0, kPerUnit, 1), opB(Vb, kd, d, 1, kPerUnit), dS, nk, k, n, k,
-                       d, 1.f, 0.f, 0, 0);
+    const Operand dOa = opA(dO, nd, d, 0, kPerUnit, 1), Vbb = opB(Vb, kd, d, 1, kPerUnit);
     if (fused) {
-        gp.epi = kEpiSoftmaxBwd;
-        gp.aux = P;
-    }
-    if (!st) st = tc_batched_gemm(gp, units, s, nullptr, 0, sms);
-    if (!st && !fused) {
-        const long long rows = (long long)units * n;
-        KernelScope scope(LINFORMER_KERNEL_BACKWARD, s);
-        softmax_bwd_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(P, dS, k, rows);
-        if (cudaPeekAtLastError() != cudaSuccess) st = LINFORMER_ERR_LAUNCH;
+        gs.epi = kEpiSoftmaxPair;
+        gs.A2 = dOa;
+        gs.B2 = Vbb;
+        gs.C2 = dS;
+        gs.alpha2 = 1.f;
+        if (!st) st = tc_batched_gemm(gs, units, s, nullptr, 0, sms);
+    } else {
+        if (!st) st = tc_batched_gemm(gs, units, s, nullptr, 0, sms);
+        if (!st) st = softmax_rows(P, p.pad, h, n, k, units, 0, s);
+        if (!st) st = tc_batched_gemm(args(dOa, Vbb, dS, nk, k, n, k, d, 1.f, 0.f, 0, 0), units, s,
+                                      nullptr, 0, sms);
+        if (!st) {
+            const long long rows = (long long)units * n;
+            KernelScope scope(LINFORMER_KERNEL_BACKWARD, s);
+            softmax_bwd_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(P, dS, k, rows);
+            if (cudaPeekAtLastError() != cudaSuccess) st = LINFORMER_ERR_LAUNCH;
+        }
     }
     // dVbar = P^T dO; dQ = dS Kbar / sqrt(d); dKbar = dS^T Q / sqrt(d)
     if (!st) st = tc_batched_gemm(args(opA(P, nk, k, 1, kPerUnit), opB(dO, nd, d, 0, kPerUnit, 1), dVb,

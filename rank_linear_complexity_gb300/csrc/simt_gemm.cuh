@@ -64,13 +64,18 @@ struct GemmArgs {
     int cblk = 0;
     long long cblk_stride = 0;
     int blk_ua = 0, blk_ub = 0;
+    // kEpiSoftmaxPair: the second output (laid out as C) and the second product's scale
+    float *C2 = nullptr;
+    float alpha2 = 1.f;
 };
 
 // What the tensor-core product writes: alpha A B (+ beta C, output masks), the row
 // softmax of alpha A B (rows at or past the unit's length zero), or
-// aux * (alpha A B - rowsum(aux * alpha A B)) (the softmax backward with aux = P).
-// The two row forms need N <= 256 (a tile holds whole rows) and no sum over units.
-enum EpilogueKind { kEpiPlain = 0, kEpiSoftmax = 1, kEpiSoftmaxBwd = 2 };
+// aux * (alpha A B - rowsum(aux * alpha A B)) (the softmax backward with aux = P), or
+// both at once from two products of each tile (kEpiSoftmaxPair: C = P = the row
+// softmax of alpha A B, C2 = P * (dP - rowsum(P * dP)) with dP = alpha2 A2 B2).
+// The row forms need N <= 256 (a tile holds whole rows) and no sum over units.
+enum EpilogueKind { kEpiPlain = 0, kEpiSoftmax = 1, kEpiSoftmaxBwd = 2, kEpiSoftmaxPair = 3 };
 
 // Operand A (M x K) or B (K x N) of a product from a stored row-major matrix: `trans`
 // says the stored matrix is the operand's transpose; nmask 1 zeroes operand rows >= L,

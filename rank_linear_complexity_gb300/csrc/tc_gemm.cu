@@ -210,6 +210,7 @@ struct Sched {
     int ksteps;              // 64-deep steps of one unit's whole K
     int usum;                // 1: z is a group; its terms i < per_group are units g * ga + i * gb
     int per_group, ga, gb, uc, terms;  // chunks of uc units; terms 2 with A2 B2
+    int pair;                // 1: two products per tile (A B, then A2 B2), one accumulator each
 };
 
 struct Item {
@@ -234,6 +235,11 @@ __device__ __forceinline__ Item item_at(const GemmArgs &g, const Sched &sc, long
         it.nk = cnt > 0 ? cnt * sc.terms * sc.ksteps : 0;
         it.kbeg = 0;
         it.kend = g.K;
+    } else if (sc.pair) {
+        it.first = 0;
+        it.kbeg = 0;
+        it.kend = g.K;
+        it.nk = 2 * sc.ksteps;
     } else {
         it.first = 0;
         it.kbeg = it.split * g.kchunk;
@@ -257,6 +263,13 @@ __device__ __forceinline__ StepSrc step_src(const GemmArgs &g, const Sched &sc, 
         const int term = rem / sc.ksteps;
         r.unit = it.z * sc.ga + i * sc.gb;
         r.k0 = (rem % sc.ksteps) * kTK;
+        r.kend = g.K;
+        r.a = term ? g.A2 : g.A;
+        r.b = term ? g.B2 : g.B;
+    } else if (sc.pair) {
+        const int term = s / sc.ksteps;
+        r.unit = it.z;
+        r.k0 = (s % sc.ksteps) * kTK;
         r.kend = g.K;
         r.a = term ? g.A2 : g.A;
         r.b = term ? g.B2 : g.B;
@@ -468,11 +481,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc
     const int N = g.N;
     float *out = g.C + (long long)it.z * g.sC;
     const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0 && (g.ldc & 3) == 0;
-    if (g.epi == kEpiSoftmax) {
-        // p = 2^(a2 s - m) / l with a2 = alpha log2(e); m and l in one pass (the running
-        // sum rescaled when the running maximum grows), p in a second
-        const float a2 = g.alpha * kLog2e;
-        float m = -INFINITY, l = 0.f;
+    // p = 2^(a2 s - m) / l with a2 = alpha log2(e): one FFMA and one ex2 a value; m and l
+    // in one pass over the scores (the running sum rescaled when the running maximum grows)
+    const float a2 = g.alpha * kLog2e;
+    auto softmax_stats = [&](float &m, float &l) {
+        m = -INFINITY;
+        l = 0.f;
         for (int c = 0; c < N; c += 32) {
             uint32_t v[32];
             fetch(c, v);
@@ -492,6 +506,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc
             l = fmaf(l, ex2_approx(m - mn), s0 + s1);
             m = mn;
         }
+    };
+    if (g.epi == kEpiSoftmax) {
+        float m, l;
+        softmax_stats(m, l);
         // rows at or past the length are exact zeros (their scores may be anything)
         const float inv = 1.f / l;
         for (int c = 0; c < N; c += 32) {
@@ -503,6 +521,94 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc
                 val[i] = (live && c + i < N) ? ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m)) * inv
                                              : 0.f;
             emit_rows32(val, out + c, g.ldc, r0, min(32, N - c), g.M, stg, lane, vec);
+        }
+        return;
+    }
+    if (g.epi == kEpiSoftmaxPair) {
+        // S in this accumulator, dP = alpha2 * the next one.  Pass 1: the row maximum of
+        // S (alpha > 0, so m = a2 max s).  Pass 2: e = 2^(a2 s - m), l = sum e and
+        // D' = sum e dP together.  Pass 3: e again, P = e / l, dS = P (dP - D'/l) written
+        // together; the two accumulators' chunks are read under one wait.
+        const uint32_t tdp = taddr + (uint32_t)BN;
+        auto fetch_dp = [&](int c, uint32_t (&v)[32]) {
+            if (acc) {
+                tmem_ld32(tdp + (uint32_t)c, v);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0u;
+            }
+        };
+        auto fetch2 = [&](int c, uint32_t (&vs)[32], uint32_t (&vd)[32]) {
+            if (acc) {
+                tmem_ld32_async(taddr + (uint32_t)c, vs);
+                tmem_ld32_async(tdp + (uint32_t)c, vd);
+                tmem_wait_ld(vs);
+                tie32(vd);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) vs[i] = vd[i] = 0u;
+            }
+        };
+        // columns at or past N: the accumulator holds zeros there (B's rows are zero), so
+        // only the maximum and the exponentials need the bound; a whole chunk (the usual
+        // case) has none.  Rows at or past the length are written as exact zeros.
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+        for (int c = 0; c < N; c += 32) {
+            uint32_t v[32];
+            fetch(c, v);
+            const int nv = N - c;
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                if (nv >= 32 || i < nv) mx0 = fmaxf(mx0, __uint_as_float(v[i]));
+                if (nv >= 32 || i + 1 < nv) mx1 = fmaxf(mx1, __uint_as_float(v[i + 1]));
+            }
+        }
+        const float m = a2 * fmaxf(mx0, mx1);
+        float l0 = 0.f, l1 = 0.f, D0 = 0.f, D1 = 0.f;
+        for (int c = 0; c < N; c += 32) {
+            uint32_t vs[32], vd[32];
+            fetch2(c, vs, vd);
+            float e[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) e[i] = ex2_approx(fmaf(a2, __uint_as_float(vs[i]), -m));
+            if (N - c < 32) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i >= N - c) e[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                l0 += e[i];
+                l1 += e[i + 1];
+                D0 = fmaf(e[i], __uint_as_float(vd[i]), D0);
+                D1 = fmaf(e[i + 1], __uint_as_float(vd[i + 1]), D1);
+            }
+        }
+        const float inv = 1.f / (l0 + l1);
+        const float D = g.alpha2 * inv * (D0 + D1);
+        float *out2 = g.C2 + (long long)it.z * g.sC;
+        for (int c = 0; c < N; c += 32) {
+            float val[32];
+            {
+                uint32_t vs[32];
+                fetch(c, vs);  // warp-wide: outside any branch on the lane's row
+                if (live) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        val[i] = ex2_approx(fmaf(a2, __uint_as_float(vs[i]), -m)) * inv;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) val[i] = 0.f;
+                }
+            }
+            emit_rows32(val, out + c, g.ldc, r0, min(32, N - c), g.M, stg, lane, vec);
+            uint32_t vd[32];
+            fetch_dp(c, vd);
+            if (live) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) val[i] *= fmaf(g.alpha2, __uint_as_float(vd[i]), -D);
+            }
+            emit_rows32(val, out2 + c, g.ldc, r0, min(32, N - c), g.M, stg, lane, vec);
         }
         return;
     }
@@ -610,11 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const GemmArgs g, 
         // ---- epilogue: TMEM accumulator -> C (or the split's partial)
         const int q = warp & 3;
         float *stg = transpose + q * 32 * kStagePitch;
+        // two accumulators alternate between tiles, or (pair) serve one tile together
+        const int bufs = sc.pair ? 1 : 2;
         int tcount = 0;
         for (long long w = blockIdx.x; w < sc.items; w += gridDim.x, ++tcount) {
             const Item it = item_at<BN>(g, sc, w);
-            const int b = tcount & 1;
-            if (!warp_wait(acc_full + b, (tcount >> 1) & 1, g.status, 33, abort_flag)) break;
+            const int b = tcount % bufs, use = tcount / bufs;
+            if (!warp_wait(acc_full + b, use & 1, g.status, 33, abort_flag)) break;
             tc_fence_after();
             if (*abort_flag) break;
             epilogue_tile<BN>(g, sc, it, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN), stg,
@@ -628,17 +736,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const GemmArgs g, 
         const uint32_t idesc = idesc_f16(kTM, BN, 1, a_mn, b_mn);
         const uint64_t sa = slice_step(a_mn), sb = slice_step(b_mn);
         uint32_t step = 0;
+        const int bufs = sc.pair ? 1 : 2;
         int tcount = 0;
         bool ok = true;
         for (long long w = blockIdx.x; ok && w < sc.items; w += gridDim.x, ++tcount) {
             const Item it = item_at<BN>(g, sc, w);
-            const int b = tcount & 1;
-            if (tcount >= 2) ok = mbar_wait(acc_empty + b, ((tcount >> 1) - 1) & 1, g.status, 34,
-                                            abort_flag);
+            const int b = tcount % bufs, use = tcount / bufs;
+            if (use >= 1) ok = mbar_wait(acc_empty + b, (use - 1) & 1, g.status, 34, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(b * BN);
             for (int s = 0; s < it.nk; ++s, ++step) {
+                // pair: the first product's steps into accumulator 0, the second's into 1
+                const int term = sc.pair ? s / sc.ksteps : 0, ks = sc.pair ? s % sc.ksteps : s;
+                const uint32_t d = tmem + (uint32_t)((sc.pair ? term : b) * BN);
                 const int st = (int)(step % C::kStages);
                 ok = mbar_wait(full + st, (step / C::kStages) & 1, g.status, 31, abort_flag);
                 if (!ok) break;
@@ -649,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const GemmArgs g, 
                                bl = tile_desc(base + 2 * C::kA + C::kB, b_mn);
 #pragma unroll
                 for (int k = 0; k < kTK / 16; ++k) {
-                    mma_ss(d, ah + k * sa, bh + k * sb, idesc, (s > 0 || k > 0) ? 1u : 0u);
+                    mma_ss(d, ah + k * sa, bh + k * sb, idesc, (ks > 0 || k > 0) ? 1u : 0u);
                     mma_ss(d, ah + k * sa, bl + k * sb, idesc, 1u);
                     mma_ss(d, al + k * sa, bh + k * sb, idesc, 1u);
                 }
@@ -710,8 +820,16 @@ int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, size_t p
         if (g.B.blk_stride & 3) g.B.vec = 0;
     }
     const int BN = g.N <= 64 ? 64 : (g.N <= 128 ? 128 : 256);
+    const bool pair = g.epi == kEpiSoftmaxPair;
     if (g.epi != kEpiPlain && (g.N > BN || usum || (g.epi == kEpiSoftmaxBwd && !g.aux)))
         return LINFORMER_ERR_SIZE;
+    if (pair) {
+        if (!g.A2.p || !g.B2.p || !g.C2 || g.A2.xfast != g.A.xfast || g.B2.xfast != g.B.xfast ||
+            !(g.alpha > 0.f))
+            return LINFORMER_ERR_SIZE;
+        set_operand_vec(g.A2, g.A2.xfast ? g.M : g.K);
+        set_operand_vec(g.B2, g.B2.xfast ? g.N : g.K);
+    }
     Sched sc{};
     sc.tiles_m = (g.M + kTM - 1) / kTM;
     sc.tiles_n = (g.N + BN - 1) / BN;
@@ -719,6 +837,7 @@ int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, size_t p
     sc.usum = usum ? 1 : 0;
     sc.zcount = usum ? g.usum_groups : units;
     sc.terms = two ? 2 : 1;
+    sc.pair = pair ? 1 : 0;
     sc.per_group = g.usum_per_group;
     sc.ga = g.usum_ga;
     sc.gb = g.usum_gb;

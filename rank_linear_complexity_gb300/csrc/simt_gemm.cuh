@@ -50,8 +50,7 @@ struct GemmArgs {
     float *part;
     int *status;  // device status word for bounded waits that run out (tensor-core kernel)
     // Tensor-core product only (tc_batched_gemm):
-    int epi = 0;                 // an EpilogueKind
-    const float *aux = nullptr;  // kEpiSoftmaxBwd: P, laid out as C
+    int epi = 0;  // an EpilogueKind
     // usum_groups > 0: a sum over units.  Output matrix g < usum_groups (C + g sC) is the
     // sum over i < usum_per_group of A_u B_u (+ A2_u B2_u when A2.p is set), unit
     // u = g usum_ga + i usum_gb, each term with its own unit's length masks; the
@@ -69,13 +68,12 @@ struct GemmArgs {
     float alpha2 = 1.f;
 };
 
-// What the tensor-core product writes: alpha A B (+ beta C, output masks), the row
-// softmax of alpha A B (rows at or past the unit's length zero), or
-// aux * (alpha A B - rowsum(aux * alpha A B)) (the softmax backward with aux = P), or
-// both at once from two products of each tile (kEpiSoftmaxPair: C = P = the row
-// softmax of alpha A B, C2 = P * (dP - rowsum(P * dP)) with dP = alpha2 A2 B2).
-// The row forms need N <= 256 (a tile holds whole rows) and no sum over units.
-enum EpilogueKind { kEpiPlain = 0, kEpiSoftmax = 1, kEpiSoftmaxBwd = 2, kEpiSoftmaxPair = 3 };
+// What the tensor-core product writes: alpha A B (+ beta C, output masks), or, from
+// two products of each row tile (kEpiSoftmaxPair), C = P = the row softmax of
+// alpha A B (rows at or past the unit's length zero) and C2 = P * (dP - rowsum(P * dP))
+// with dP = alpha2 A2 B2.  The pair needs N <= 256 (a tile holds whole rows),
+// alpha > 0 and no sum over units.
+enum EpilogueKind { kEpiPlain = 0, kEpiSoftmaxPair = 1 };
 
 // Operand A (M x K) or B (K x N) of a product from a stored row-major matrix: `trans`
 // says the stored matrix is the operand's transpose; nmask 1 zeroes operand rows >= L,
@@ -103,8 +101,8 @@ int batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part = nullptr,
 // of each term), with the epilogue forms and sums over units of GemmArgs.  With `part`
 // (part_floats floats) a plain product may split K (a sum over units, its units) for
 // about four work items per SM; partials are added in split order.  Returns
-// LINFORMER_OK, LINFORMER_ERR_SIZE (a row form with N > 256 or a sum, mismatched second
-// operands) or LINFORMER_ERR_LAUNCH.
+// LINFORMER_OK, LINFORMER_ERR_SIZE (a pair with N > 256 or a sum, mismatched second
+// operands, blocks that break the rules of Operand.xblk) or LINFORMER_ERR_LAUNCH.
 int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part = nullptr,
                     size_t part_floats = 0, int sms = 0,
                     int kernel_id = LINFORMER_KERNEL_BACKWARD);

@@ -5,9 +5,9 @@
 // length read as zero), and two further forms the backward of the Linformer attention
 // needs ("Linformer(Self-Attention with Linear Complexity) 요약 설명", section Model:
 // the forward's definition; the gradients are its chain rule):
-//   - a fused epilogue: C = the row softmax of alpha A B (P from the scores), or
-//     C = Paux * (alpha A B - rowsum(Paux * alpha A B)) (dS from dP), the tile holding
-//     whole rows;
+//   - a pair item: S = alpha A B and dP = alpha2 A2 B2 of one row tile in two
+//     accumulators, the epilogue writing P = the row softmax of S (C) and
+//     dS = P (dP - rowsum(P dP)) (C2), the tile holding whole rows;
 //   - a sum over units: output matrix g = sum over the units u of its group of A_u B_u
 //     (+ A2_u B2_u), the gradient of a projection matrix shared by those units.
 //
@@ -357,29 +357,6 @@ __device__ __forceinline__ bool put_step(const Frag<kTM> &fa, const Frag<BN> &fb
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Eight 4-float groups of columns c .. c + 31 of one row (row pointer `row`, `cols`
-// columns): 16-byte loads when the row allows them, zero past the row's end.
-__device__ __forceinline__ void load_row32(float4 (&p)[8], const float *row, int c, int cols,
-                                           bool vec) {
-    if (vec && c + 32 <= cols) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) p[j] = __ldg(reinterpret_cast<const float4 *>(row + c + 4 * j));
-        return;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int q = c + 4 * j;
-        p[j].x = q < cols ? __ldg(row + q) : 0.f;
-        p[j].y = q + 1 < cols ? __ldg(row + q + 1) : 0.f;
-        p[j].z = q + 2 < cols ? __ldg(row + q + 2) : 0.f;
-        p[j].w = q + 3 < cols ? __ldg(row + q + 3) : 0.f;
-    }
-}
-__device__ __forceinline__ float pick(const float4 (&p)[8], int i) {
-    const float4 q = p[i >> 2];
-    return (i & 3) == 0 ? q.x : ((i & 3) == 1 ? q.y : ((i & 3) == 2 ? q.z : q.w));
-}
-
 // The warp's output of one 32-column chunk of rows r0 .. r0 + 31 (lane l holds row
 // r0 + l in val): each lane writes its row into the warp's staging rows (kStagePitch
 // floats apart: a quarter-warp's 16-byte stores or loads fall in distinct banks), then
@@ -475,60 +452,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc
         }
         return;
     }
-    // Whole rows (col0 = 0, N <= BN).
+    // kEpiSoftmaxPair, whole rows (col0 = 0, N <= BN): S in this accumulator, dP =
+    // alpha2 * the next one; p = 2^(a2 s - m) / l with a2 = alpha log2(e), one FFMA and
+    // one ex2 a value.  Pass 1: the row maximum of S (alpha > 0, so m = a2 max s).
+    // Pass 2: e = 2^(a2 s - m), l = sum e and D' = sum e dP together (the two
+    // accumulators' chunks read under one wait).  Pass 3: e again, P = e / l and
+    // dS = P (dP - D'/l) written together.
     const int L = tc_unit_length(g.pad, it.z, g.h, g.n);
     const bool live = row < L;
     const int N = g.N;
     float *out = g.C + (long long)it.z * g.sC;
     const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0 && (g.ldc & 3) == 0;
-    // p = 2^(a2 s - m) / l with a2 = alpha log2(e): one FFMA and one ex2 a value; m and l
-    // in one pass over the scores (the running sum rescaled when the running maximum grows)
     const float a2 = g.alpha * kLog2e;
-    auto softmax_stats = [&](float &m, float &l) {
-        m = -INFINITY;
-        l = 0.f;
-        for (int c = 0; c < N; c += 32) {
-            uint32_t v[32];
-            fetch(c, v);
-            float cm0 = -INFINITY, cm1 = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                if (c + i < N) cm0 = fmaxf(cm0, a2 * __uint_as_float(v[i]));
-                if (c + i + 1 < N) cm1 = fmaxf(cm1, a2 * __uint_as_float(v[i + 1]));
-            }
-            const float mn = fmaxf(m, fmaxf(cm0, cm1));
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                if (c + i < N) s0 += ex2_approx(fmaf(a2, __uint_as_float(v[i]), -mn));
-                if (c + i + 1 < N) s1 += ex2_approx(fmaf(a2, __uint_as_float(v[i + 1]), -mn));
-            }
-            l = fmaf(l, ex2_approx(m - mn), s0 + s1);
-            m = mn;
-        }
-    };
-    if (g.epi == kEpiSoftmax) {
-        float m, l;
-        softmax_stats(m, l);
-        // rows at or past the length are exact zeros (their scores may be anything)
-        const float inv = 1.f / l;
-        for (int c = 0; c < N; c += 32) {
-            uint32_t v[32];
-            fetch(c, v);
-            float val[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                val[i] = (live && c + i < N) ? ex2_approx(fmaf(a2, __uint_as_float(v[i]), -m)) * inv
-                                             : 0.f;
-            emit_rows32(val, out + c, g.ldc, r0, min(32, N - c), g.M, stg, lane, vec);
-        }
-        return;
-    }
-    if (g.epi == kEpiSoftmaxPair) {
-        // S in this accumulator, dP = alpha2 * the next one.  Pass 1: the row maximum of
-        // S (alpha > 0, so m = a2 max s).  Pass 2: e = 2^(a2 s - m), l = sum e and
-        // D' = sum e dP together.  Pass 3: e again, P = e / l, dS = P (dP - D'/l) written
-        // together; the two accumulators' chunks are read under one wait.
+    {
         const uint32_t tdp = taddr + (uint32_t)BN;
         auto fetch_dp = [&](int c, uint32_t (&v)[32]) {
             if (acc) {
@@ -611,53 +547,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs &g, const Sched &sc
             emit_rows32(val, out2 + c, g.ldc, r0, min(32, N - c), g.M, stg, lane, vec);
         }
         return;
-    }
-    // kEpiSoftmaxBwd: dS = P (dP - D), dP = alpha * accumulator, D = sum_j P_j dP_j, with
-    // the lane reading its own row of P (whole 128-byte lines), the next 32 columns in
-    // flight while the current ones are used.
-    const float *prow = g.aux + (long long)it.z * g.sC + (long long)(row_ok ? row : r0) * g.ldc;
-    const int pcols = row_ok ? N : 0;
-    const bool pvec = (g.ldc & 3) == 0 && ((reinterpret_cast<uintptr_t>(g.aux) & 15) == 0) &&
-                      ((g.sC & 3) == 0);
-    float4 pa[8], pb[8];
-    float D0 = 0.f, D1 = 0.f;
-    load_row32(pa, prow, 0, pcols, pvec);
-    for (int c = 0; c < N; c += 64) {
-        const bool second = c + 32 < N;
-        if (second) load_row32(pb, prow, c + 32, pcols, pvec);
-        uint32_t v[32];
-        fetch(c, v);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            D0 = fmaf(pick(pa, i), __uint_as_float(v[i]), D0);
-            D1 = fmaf(pick(pa, i + 1), __uint_as_float(v[i + 1]), D1);
-        }
-        if (!second) break;
-        if (c + 64 < N) load_row32(pa, prow, c + 64, pcols, pvec);
-        fetch(c + 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            D0 = fmaf(pick(pb, i), __uint_as_float(v[i]), D0);
-            D1 = fmaf(pick(pb, i + 1), __uint_as_float(v[i + 1]), D1);
-        }
-    }
-    const float D = g.alpha * (D0 + D1);
-    auto emit = [&](const float4 (&pp)[8], int c) {
-        uint32_t v[32];
-        fetch(c, v);
-        float val[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) val[i] = pick(pp, i) * fmaf(g.alpha, __uint_as_float(v[i]), -D);
-        emit_rows32(val, out + c, g.ldc, r0, min(32, N - c), g.M, stg, lane, vec);
-    };
-    load_row32(pa, prow, 0, pcols, pvec);
-    for (int c = 0; c < N; c += 64) {
-        const bool second = c + 32 < N;
-        if (second) load_row32(pb, prow, c + 32, pcols, pvec);
-        emit(pa, c);
-        if (!second) break;
-        if (c + 64 < N) load_row32(pa, prow, c + 64, pcols, pvec);
-        emit(pb, c + 32);
     }
 }
 
@@ -821,7 +710,7 @@ int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, size_t p
     }
     const int BN = g.N <= 64 ? 64 : (g.N <= 128 ? 128 : 256);
     const bool pair = g.epi == kEpiSoftmaxPair;
-    if (g.epi != kEpiPlain && (g.N > BN || usum || (g.epi == kEpiSoftmaxBwd && !g.aux)))
+    if (g.epi != kEpiPlain && (g.epi != kEpiSoftmaxPair || g.N > BN || usum))
         return LINFORMER_ERR_SIZE;
     if (pair) {
         if (!g.A2.p || !g.B2.p || !g.C2 || g.A2.xfast != g.A.xfast || g.B2.xfast != g.B.xfast ||

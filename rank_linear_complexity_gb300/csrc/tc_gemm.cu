@@ -23,13 +23,13 @@
 //     64-deep step from global memory, coalesced along each operand's contiguous axis,
 //     split them and write hi and lo into a ring of shared-memory stages in the
 //     128-byte-swizzled layout the MMA reads (K-major when the operand's K axis is
-//     contiguous in memory, MN-major when its M or N axis is); with BN = 64 the loads of
-//     the next step are in flight while the current one is split and stored;
+//     contiguous in memory, MN-major when its M or N axis is); a step's loads stay in
+//     flight while its producers wait for a free stage;
 //   - one thread issues the twelve MMAs of a step (four 16-deep slices, three products
 //     each) into one of two TMEM accumulators of BN fp32 columns, the tiles alternating;
-//   - four epilogue warps (TMEM lane quarters 0..3) drain the other accumulator through
-//     a small shared-memory transpose, so that every fp32 store of C (or of a split's
-//     partial) is a whole 128-byte line.
+//   - four epilogue warps (TMEM lane quarters 0..3) drain the other accumulator, each
+//     lane its row, through staging rows in shared memory, so that every fp32 store
+//     instruction of C (or of a split's partial) writes four whole 128-byte row pieces.
 // So the loads of later steps, the products and the stores of earlier tiles overlap.
 // Every wait is bounded (the status word gets 31..34 and the roles stop).
 #include <cuda_bf16.h>

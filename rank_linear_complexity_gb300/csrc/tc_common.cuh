@@ -142,18 +142,30 @@ inline ProjPlan plan_projection(int n, int64_t members, int64_t groups, int mhal
     return pl;
 }
 
-// After the main loop the projection reuses its ring: the split reduction's two 32 KB
-// slice buffers at [0, 64 KB) and, in four-warp launches, a 32 KB image staging buffer
-// at [64 KB, 96 KB); eight-warp launches stage in [0, 128 KB) (two groups, two buffers
-// each).  Every plan above gives at least 96 KB, and 192 KB to eight-warp launches.
+// After the main loop the projection reuses its ring: the split reduction's three 32 KB
+// slice buffers at [0, 96 KB), then, in four-warp launches, two 32 KB image staging
+// buffers at [0, 64 KB); eight-warp launches stage in [0, 128 KB) (two groups, two
+// buffers each).  Every plan above gives at least 96 KB, and 192 KB to eight-warp launches.
 constexpr size_t kProjectMinRing = 96 * 1024;
 constexpr size_t kProjectMinRingWide = 128 * 1024;
+
+// Arrival counters of a unit whose sequence is split into C chunks: one for the unit,
+// one per group of chunks (the two-level reduction of tc_project.cu).  Groups hold
+// split_group(C) chunks: all C below 9 (one level: the second level's extra store and
+// arrival cost more than it saves there), else ceil(sqrt(C)); C <= 64 gives at most 8.
+constexpr int kCountersPerUnit = 9;
+__host__ __device__ inline int split_group(int C) {
+    if (C < 9) return C;
+    int g = 1;
+    while (g * g < C) ++g;
+    return g;
+}
 
 struct ProjParams {
     const int32_t *pad;
     float *partial;      // see partial_bytes (used when C > 1)
     uint8_t *images;     // [units][4][kpad * 128 bytes]
-    int *counters;       // [units], zero on entry, left zero on exit
+    int *counters;       // [units][kCountersPerUnit], zero on entry, left zero on exit
     int *info;           // [units]
     float *kbar_out;     // optional fp32 [units][k][64]
     float *vbar_out;     // optional fp32 [units][k][64]

@@ -81,7 +81,8 @@ int plan_forward(const Problem &p, size_t part_budget, ForwardPlan *fp) {
     f.members = f.per_head ? p.b : f.units;
     f.groups = f.units / f.members;
     f.img = up256(f.units * 4 * image_bytes(f.kpad));
-    f.cnt = up256((f.units + 1) * sizeof(int));  // + the product-count summary word
+    // per unit the split reduction's arrival counters, + the product-count summary word
+    f.cnt = up256((f.units * kCountersPerUnit + 1) * sizeof(int));
     if (part_budget != ~size_t(0)) {  // a fixed workspace: images, counters and info first
         if (f.img + 2 * f.cnt > part_budget) return LINFORMER_ERR_SIZE;
         part_budget -= f.img + 2 * f.cnt;
@@ -123,7 +124,7 @@ int run_forward(const Problem &p, const ForwardPlan &f, char *ws, float *Kbar_ou
     pp.partial = partial;
     pp.images = images;
     pp.counters = counters;
-    pp.terms_seen = counters + units;
+    pp.terms_seen = counters + units * kCountersPerUnit;
     pp.info = info;
     pp.kbar_out = Kbar_out;
     pp.vbar_out = Vbar_out;
@@ -161,7 +162,7 @@ int run_forward(const Problem &p, const ForwardPlan &f, char *ws, float *Kbar_ou
     ap.out = p.O;
     ap.images = images;
     ap.info = info;
-    ap.terms_seen = counters + units;
+    ap.terms_seen = counters + units * kCountersPerUnit;
     ap.status = status;
     ap.h = p.h;
     ap.n = p.n;

@@ -14,11 +14,12 @@
 // the images the attention step reads, with four warps, or with eight (Kbar and Vbar
 // in parallel) when the launch runs one CTA per SM.
 //
-// Chunks of the same unit are summed in a fixed order (chunk 0, 1, ...) by
-// whichever CTA of the unit arrives last, so the result does not depend on
-// scheduling.  That CTA pulls the other chunks' sums in as 32 KB slices by bulk
-// copy, converts to the split images the attention step reads and picks the
-// number of P.Vbar products from max|Vbar|.
+// Chunks of the same unit are summed in a fixed order, so the result does not depend
+// on scheduling: in groups of chunks (chunk order) by the last CTA of each group to
+// arrive, then the groups' sums (group order) by the last group to arrive (one level
+// below 9 chunks).  Those CTAs pull the other sums in as 32 KB slices by bulk copy; the
+// last one converts to the split images the attention step reads and picks the number
+// of P.Vbar products from max|Vbar|.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -104,8 +105,8 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
-    uint64_t *fin = acc_full + 1;  // two slice buffers of the split reduction
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 2);
+    uint64_t *fin = acc_full + 1;  // three slice buffers of the split reduction
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 3);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 2);
     float *red = reinterpret_cast<float *>(tmem_slot + 4);
@@ -118,8 +119,7 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
             mbar_init(empty + s, 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(fin, 1);
-        mbar_init(fin + 1, 1);
+        for (int i = 0; i < 3; ++i) mbar_init(fin + i, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_mbar_init();
@@ -382,16 +382,25 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                 if (jl == 0) {
                     p.info[uu] = pack_info(terms, e);
                     atomicOr(p.terms_seen, 1 << terms);
-                    p.counters[uu] = 0;
                 }
                 named_barrier_sync(1, 128);  // red[] is reused by the next unit
             }
         }
         if (gt == 0) bulk_wait0();  // the images are written before the CTA exits
     } else {
-    if (!aborted && Cu > 1) {
-        // This chunk's sums, [half of k_pad][column][row]: a warp stores 128 contiguous bytes.
-        float *mine = p.partial + ((size_t)u * p.C + c) * p.mhalves * 2 * kSlice;
+    // ---- Split units: the chunk sums are added in a fixed order, in two levels.  Chunk c
+    // belongs to group c / G (G = split_group(Cu), chunks in the unit's order); the last CTA
+    // of a group to arrive adds the group's chunks in chunk order and leaves the sum in its
+    // TMEM; with more than one group it also stores that sum in the slot of the group's
+    // first chunk, and the last group to arrive adds the groups' sums in group order.
+    // Whichever CTAs arrive last, every sum is formed in the same order, so the result does
+    // not depend on scheduling; the longest chain of slices one CTA reads is about
+    // 2 sqrt(Cu) chunks instead of Cu - 1.
+    // A chunk's sums in the partial buffer: [half of k_pad][column][row] (a warp stores 128
+    // contiguous bytes); the other chunks' sums come in as 32 KB slices (one 64-column half
+    // of one 128-row block) by bulk copy into three shared buffers (the ring is idle).
+    auto store_partial = [&](int slot) {
+        float *dst = p.partial + ((size_t)u * p.C + slot) * p.mhalves * 2 * kSlice;
 #pragma unroll 1
         for (int mh = 0; mh < p.mhalves; ++mh) {
 #pragma unroll 1
@@ -400,25 +409,124 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                 tmem_ld32(lane_base + mh * 128 + cc * 32, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    mine[(size_t)mh * 2 * kSlice + (cc * 32 + i) * 128 + jl] = __uint_as_float(v[i]);
+                    dst[(size_t)mh * 2 * kSlice + (cc * 32 + i) * 128 + jl] = __uint_as_float(v[i]);
             }
         }
+    };
+    constexpr int kSliceBufs = 3;
+    float *sbuf = reinterpret_cast<float *>(smem);
+    int sl_issued = 0, sl_used = 0;  // slices started (thread 0's count) and consumed, per CTA
+    // Adds, for each M-half and column half, the sums of chunks src(0 .. npos - 1) in that
+    // order, position `own` being this CTA's TMEM; the result goes back to TMEM.
+    auto reduce = [&](int npos, int own, int first, int stride) -> bool {
+        const int per = npos - 1;
+        const int nslices = p.mhalves * 2 * per;
+        auto slice_src = [&](int idx) {
+            const int mh = idx / (2 * per), rem = idx % (2 * per);
+            const int half = rem / per, k2 = rem % per;
+            const int pos = k2 < own ? k2 : k2 + 1;
+            return p.partial + (((size_t)u * p.C + first + pos * stride) * p.mhalves + mh) * 2 * kSlice +
+                   half * kSlice;
+        };
+        const int base = sl_used;  // slice index of this call's first slice
+        if (tid == 0) {
+            fence_proxy_async_global();
+            for (int i = 0; i < kSliceBufs && i < nslices; ++i, ++sl_issued) {
+                const int b = sl_issued % kSliceBufs;
+                mbar_arrive_expect_tx(fin + b, kSlice * 4);
+                bulk_load(sbuf + b * kSlice, slice_src(i), kSlice * 4, fin + b);
+            }
+        }
+        bool ok = true;
+#pragma unroll 1
+        for (int mh = 0; mh < p.mhalves; ++mh) {
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t tcol = lane_base + mh * 128 + half * 64;
+                float acc[64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+#pragma unroll 1
+                for (int pos = 0; pos < npos; ++pos) {
+                    if (pos == own) {
+                        uint32_t v[64];
+                        tmem_ld64(tcol, v);
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) acc[i] += __uint_as_float(v[i]);
+                        continue;
+                    }
+                    const int b = sl_used % kSliceBufs;
+                    if (!mbar_wait(fin + b, (sl_used / kSliceBufs) & 1, p.status, 15, abort_flag)) ok = false;
+                    const float *sb = sbuf + b * kSlice;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) acc[i] += sb[i * 128 + jl];
+                    __syncthreads();
+                    const int next = sl_used - base + kSliceBufs;  // this call's slice to start next
+                    if (tid == 0 && ok && next < nslices) {
+                        mbar_arrive_expect_tx(fin + b, kSlice * 4);
+                        bulk_load(sbuf + b * kSlice, slice_src(next), kSlice * 4, fin + b);
+                        ++sl_issued;
+                    }
+                    ++sl_used;
+                }
+                uint32_t w0[32], w1[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    w0[i] = __float_as_uint(acc[i]);
+                    w1[i] = __float_as_uint(acc[32 + i]);
+                }
+                tmem_st32(tcol, w0);
+                tmem_st32(tcol + 32, w1);
+            }
+        }
+        if (tid == 0)  // copies that were started but not consumed (only after an abort)
+            for (int i = sl_used; i < sl_issued; ++i)
+                mbar_wait_drain(fin + (i % kSliceBufs), (i / kSliceBufs) & 1);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        return ok;
+    };
+    bool finish = Cu == 1;  // this CTA writes the unit's images
+    int *ucnt = p.counters + (size_t)u * kCountersPerUnit;
+    if (!aborted && Cu > 1) {
+        const int G = split_group(Cu), ng = (Cu + G - 1) / G, gi = c / G;
+        const int g0 = gi * G, gn = min(Cu, g0 + G) - g0;
+        store_partial(c);
         __threadfence();
         __syncthreads();
-        if (tid == 0) *last_flag = (atomicAdd(p.counters + u, 1) == Cu - 1) ? 1 : 0;
+        if (tid == 0) {
+            *last_flag = (atomicAdd(ucnt + 1 + gi, 1) == gn - 1) ? 1 : 0;
+            __threadfence();  // the other chunks' stores are seen before their sums are read
+        }
         __syncthreads();
+        bool last = *last_flag != 0;
+        if (last && gn > 1) last = reduce(gn, c - g0, g0, 1);
+        if (last && ng == 1) {
+            finish = true;
+        } else if (last) {
+            store_partial(g0);
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                *last_flag = (atomicAdd(ucnt, 1) == ng - 1) ? 1 : 0;
+                __threadfence();
+            }
+            __syncthreads();
+            if (*last_flag) finish = reduce(ng, gi, 0, G);
+        }
     }
 
     // Images leave through shared memory: all 128 threads put one M-half of two images
-    // (hi and lo, 16 KB each) at [64 KB, 96 KB) of the idle ring, in the images' own
-    // layout (the split reduction's slice buffers take [0, 64 KB)), and thread 0 copies
-    // them out with two bulk stores (whole lines rather than 16-byte pieces of 32 rows
-    // per store instruction).
+    // (hi and lo, 16 KB each) into one of two 32 KB buffers of the idle ring (the sums are
+    // complete by now), in the images' own layout, and thread 0 copies them out with two
+    // bulk stores (whole lines rather than 16-byte pieces of 32 rows per store
+    // instruction); a buffer is reused once the stores of two steps back have read it.
     int staged = 0;  // bulk groups thread 0 has committed
     auto stage_claim = [&]() -> uint8_t * {
-        if (tid == 0 && staged > 0) bulk_wait_read0();
+        if (tid == 0 && staged > 1) bulk_wait_read1();
         __syncthreads();
-        return smem + 65536;
+        return smem + 32768 * (staged & 1);
     };
     auto stage_flush = [&](uint8_t *stg, uint8_t *img_hi, uint8_t *img_lo, int mh) {
         const int rows = min(128, p.kpad - 128 * mh);
@@ -433,120 +541,56 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
         ++staged;
     };
     // Images, info word and product count of each unit of the CTA (a pair of units
-    // only ever comes unsplit).
+    // only ever comes unsplit), from the sums in TMEM (rows past k are zero there).
 #pragma unroll 1
     for (int us = 0; us < nunits; ++us) {
-        if (aborted || !(Cu == 1 || *last_flag)) break;
+        if (aborted || !finish || *abort_flag) break;
         const int uu = us ? u_b : u;
         const uint32_t ucol = (uint32_t)us * 128u;  // the unit's columns within an M-half
-        __threadfence();
-        // The other chunks' sums come in as 32 KB slices (one 64-column half of one
-        // 128-row block) by bulk copy into two shared buffers (the stages are idle);
-        // they are added in chunk order 0, 1, ... whatever chunk this CTA owns.
-        float *sbuf = reinterpret_cast<float *>(smem);
-        const int per = Cu - 1;
-        const int nslices = p.mhalves * 2 * per;
-        auto slice_src = [&](int idx) {
-            const int mh = idx / (2 * per), rem = idx % (2 * per);
-            const int half = rem / per, k2 = rem % per;
-            const int c2 = k2 < c ? k2 : k2 + 1;
-            return p.partial + (((size_t)uu * p.C + c2) * p.mhalves + mh) * 2 * kSlice + half * kSlice;
-        };
-        int sl_issued = 0;  // slice copies started (thread 0's count)
-        if (tid == 0 && nslices > 0) {
-            fence_proxy_async_global();
-            for (int i = 0; i < 2 && i < nslices; ++i, ++sl_issued) {
-                mbar_arrive_expect_tx(fin + i, kSlice * 4);
-                bulk_load(sbuf + i * kSlice, slice_src(i), kSlice * 4, fin + i);
-            }
-        }
         uint8_t *img = p.images + (size_t)uu * 4 * image_bytes(p.kpad);
-        int sidx = 0;
-        float vmax = 0.f;
-        bool ok = true;
+        // Kbar: bf16 hi + bf16 lo images
 #pragma unroll 1
         for (int mh = 0; mh < p.mhalves; ++mh) {
             const int j = mh * 128 + jl;
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                const uint32_t tcol = lane_base + mh * 128 * nunits + ucol + half * 64;
-                float acc[64];
+            uint32_t v[64];
+            tmem_ld64(lane_base + mh * 128 * nunits + ucol, v);
+            uint8_t *stg = stage_claim();
+            if (j < p.kpad) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-#pragma unroll 1
-                for (int c2 = 0; c2 < Cu; ++c2) {
-                    if (c2 == c) {
-                        if (nkb) {
-                            uint32_t v[64];
-                            tmem_ld64(tcol, v);
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t hi[4], lo[4];
 #pragma unroll
-                            for (int i = 0; i < 64; ++i) acc[i] += __uint_as_float(v[i]);
-                        }
-                        continue;
-                    }
-                    const int b = sidx & 1;
-                    if (!mbar_wait(fin + b, (sidx >> 1) & 1, p.status, 15, abort_flag)) ok = false;
-                    const float *sb = sbuf + b * kSlice;
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) acc[i] += sb[i * 128 + jl];
-                    __syncthreads();
-                    if (tid == 0 && ok && sidx + 2 < nslices) {
-                        mbar_arrive_expect_tx(fin + b, kSlice * 4);
-                        bulk_load(sbuf + b * kSlice, slice_src(sidx + 2), kSlice * 4, fin + b);
-                        ++sl_issued;
-                    }
-                    ++sidx;
-                }
-                if (j >= p.k) {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-                }
-                if (half == 0) {  // Kbar: bf16 hi + bf16 lo images, staged (see stage_claim)
-                    uint8_t *stg = stage_claim();
-                    if (j < p.kpad) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            uint32_t hi[4], lo[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float x0 = acc[q * 8 + 2 * e], x1 = acc[q * 8 + 2 * e + 1];
-                                const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-                                const float2 hf = __bfloat1622float2(h);  // exact
-                                const float r0 = x0 - hf.x, r1 = x1 - hf.y;
-                                hi[e] = *reinterpret_cast<const uint32_t *>(&h);
-                                lo[e] = pack_bf16(r0, r1);
-                                if (kOut && p.kbar_out && j < p.k) {
-                                    float *o = p.kbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e;
-                                    o[0] = hf.x + __bfloat162float(__float2bfloat16_rn(r0));
-                                    o[1] = hf.y + __bfloat162float(__float2bfloat16_rn(r1));
-                                }
-                            }
-                            *image_chunk(stg, jl, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float x0 = j < p.k ? __uint_as_float(v[q * 8 + 2 * e]) : 0.f;
+                        const float x1 = j < p.k ? __uint_as_float(v[q * 8 + 2 * e + 1]) : 0.f;
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                        const float2 hf = __bfloat1622float2(h);  // exact
+                        const float r0 = x0 - hf.x, r1 = x1 - hf.y;
+                        hi[e] = *reinterpret_cast<const uint32_t *>(&h);
+                        lo[e] = pack_bf16(r0, r1);
+                        if (kOut && p.kbar_out && j < p.k) {
+                            float *o = p.kbar_out + ((size_t)uu * p.k + j) * kD + q * 8 + 2 * e;
+                            o[0] = hf.x + __bfloat162float(__float2bfloat16_rn(r0));
+                            o[1] = hf.y + __bfloat162float(__float2bfloat16_rn(r1));
                         }
                     }
-                    stage_flush(stg, img, img + image_bytes(p.kpad), mh);
-                } else {  // Vbar: max|Vbar| first; the images need the unit-wide scale
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        vmax = fmaxf(vmax, fmaxf(fabsf(acc[i]), fabsf(acc[32 + i])));
-                    if (Cu > 1) {  // park the summed chunks in TMEM (unsplit: TMEM holds
-                                   // them already, rows past k zero since E's are)
-                        uint32_t w0[32], w1[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            w0[i] = __float_as_uint(acc[i]);
-                            w1[i] = __float_as_uint(acc[32 + i]);
-                        }
-                        tmem_st32(tcol, w0);
-                        tmem_st32(tcol + 32, w1);
-                    }
+                    *image_chunk(stg, jl, q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *image_chunk(stg + 16384, jl, q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
+            stage_flush(stg, img, img + image_bytes(p.kpad), mh);
         }
-        if (tid == 0)  // copies that were started but not consumed (only after an abort)
-            for (int i = sidx; i < sl_issued; ++i) mbar_wait_drain(fin + (i & 1), (i >> 1) & 1);
         // Unit-wide max|Vbar| -> scale exponent and number of P.Vbar products.
+        float vmax = 0.f;
+#pragma unroll 1
+        for (int mh = 0; mh < p.mhalves; ++mh) {
+            uint32_t v[64];
+            tmem_ld64(lane_base + mh * 128 * nunits + ucol + 64, v);
+            if (mh * 128 + jl < p.k) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) vmax = fmaxf(vmax, fabsf(__uint_as_float(v[i])));
+            }
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
         if (lane == 0) red[warp] = vmax;
@@ -569,8 +613,8 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2) {
-                        const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
-                        const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
+                        const float x0 = j < p.k ? __uint_as_float(v[q * 8 + 2 * e2]) * vscale : 0.f;
+                        const float x1 = j < p.k ? __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale : 0.f;
                         const __half2 h = __floats2half2_rn(x0, x1);
                         const float2 hf = __half22float2(h);  // exact
                         const float r0 = x0 - hf.x, r1 = x1 - hf.y;
@@ -591,12 +635,12 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
             stage_flush(stg, img + 2 * image_bytes(p.kpad),
                         terms >= 2 ? img + 3 * image_bytes(p.kpad) : nullptr, mh);
         }
-        if (tid == 0 && ok) {
+        if (tid == 0) {
             p.info[uu] = pack_info(terms, e);
             atomicOr(p.terms_seen, 1 << terms);
-            p.counters[uu] = 0;
+            for (int i = 0; i < kCountersPerUnit; ++i) p.counters[(size_t)uu * kCountersPerUnit + i] = 0;
         }
-            __syncthreads();  // red[] is reused by the next unit
+        __syncthreads();  // red[] is reused by the next unit
     }
     if (tid == 0 && staged > 0) bulk_wait0();  // the images are written before the CTA exits
     }  // four-warp epilogue

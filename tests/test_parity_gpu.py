@@ -224,6 +224,25 @@ def test_pv_products_match_oracle(terms, vscale):
     check(host64(O), ref, BF16, f"terms={terms} vscale={vscale}")
 
 
+# --- scores that grow along the keys ---------------------------------------------------
+
+@pytest.mark.parametrize("mode", [PER_HEAD, HEADWISE])
+@pytest.mark.parametrize("k", [128, 200, 256])
+def test_scores_growing_along_the_keys(mode, k):
+    """Rows of E scaled by 1, 4, 16, 64 for the first, second, ... 32-key chunk of each
+    128-key half: every chunk's maximum score lies far above the previous chunks' (more
+    than 2^15 in exp2 terms), so each half's maximum sits in its last chunk and nearly
+    all of a row's weight on a few keys.  F is left alone (one P.Vbar product)."""
+    b, h, n, d = 2, 3, 512, 64
+    x = case_inputs(b, h, n, d, k, mode, BF16, seed=44)
+    j = torch.arange(k)
+    factor = torch.pow(4.0, torch.clamp((j % 128) // 32, max=3).float())  # exact in bf16
+    x["E"] = (x["E"].float() * factor.view(*([1] * (x["E"].dim() - 2)), k, 1)).to(x["E"].dtype)
+    ref = oracle_full(x, mode)
+    O = run(x, mode, BF16)
+    check(host64(O), ref, BF16, f"growing scores k={k} mode={mode}")
+
+
 # --- the five evaluation workloads at full size, whole output ------------------------
 
 def _report(entry):

@@ -686,6 +686,344 @@ int launch_tc_gemm(const GemmArgs &g, const Sched &sc, int sms, cudaStream_t s, 
     return LINFORMER_OK;
 }
 
+// ------------------------------------------------------------------ the pair kernel
+// kEpiSoftmaxPair specialised for d <= 64 with 16-byte-aligned K-major operands (the
+// backward's Q, dO, Kbar and Vbar): a CTA walks a contiguous range of row tiles, so
+// consecutive tiles share their unit and its Kbar and Vbar (B operands, N x 64 each)
+// stay in shared memory, split once per unit; the producers only read each tile's Q and
+// dO.  That frees four producer warps for the epilogue, which the pair item is bound by:
+// eight epilogue warps, two per TMEM lane quarter, each taking 128 of the 256 columns of
+// its 32 rows and exchanging the row maximum, sum and sum e dP with its partner through
+// shared memory.  S and dP fill the 512 TMEM columns, so a tile's products wait for the
+// previous tile's epilogue to have read them.
+constexpr int kPairProducerWarps = 4;
+constexpr int kPairEpiWarp0 = 4;  // warps 4..11: lane quarter w % 4, column half (w - 4) / 4
+constexpr int kPairMmaWarp = 12;
+constexpr int kPairThreads = (kPairMmaWarp + 1) * 32;  // 416
+constexpr uint32_t kPairImg = 256 * 128;               // a 256-row K-major bf16 tile (32 KB)
+constexpr uint32_t kPairTile = kTM * 128;              // a 128-row tile (16 KB)
+constexpr uint32_t kPairStg = 32 * 32 * 4;             // a warp's staging rows (swizzled)
+constexpr size_t kPairSmem = 1024 + 4 * kPairImg + 4 * kPairTile + 8 * kPairStg + 256;
+static_assert(kPairSmem <= 227 * 1024, "shared memory of one CTA");
+static_assert(kPairEpiWarp0 % 4 == 0, "epilogue warp w reads TMEM lanes 32 (w % 4) ..");
+
+// Rows x0 .. x0 + 8 nb of a row-major fp32 matrix m (row stride ld; rows >= X, and rows
+// >= L when masked, read as zero; the K <= 64 valid columns, K % 4 == 0), split into hi
+// and lo K-major tiles (128-byte rows, swizzled) by the 128 producer threads: thread t
+// takes columns 4 (t % 16) .. of rows t / 16 + 8 j, eight rows' loads in flight at once.
+__device__ __forceinline__ void pair_load_rows(const float *m, long long ld, int x0, int nb, int X,
+                                               int K, int L, bool mask, uint8_t *hi, uint8_t *lo,
+                                               int tid) {
+    const int kc = (tid % 16) * 4;
+    const bool kin = kc < K;
+#pragma unroll 1
+    for (int b0 = 0; b0 < nb; b0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int row = tid / 16 + 8 * (b0 + j), x = x0 + row;
+            const bool in = kin && x < X && !(mask && x >= L);
+            v[j] = in ? __ldg(reinterpret_cast<const float4 *>(m + (long long)x * ld + kc))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int row = tid / 16 + 8 * (b0 + j);
+            uint2 h, l;
+            split4(v[j], h, l);
+            const uint32_t off = kmajor_off(row, kc);
+            *reinterpret_cast<uint2 *>(hi + off) = h;
+            *reinterpret_cast<uint2 *>(lo + off) = l;
+        }
+    }
+}
+
+// The warp's output of one 32-column chunk of rows r0 .. r0 + 31 (lane l holds row r0 + l):
+// each lane writes its row into the warp's staging rows (128 bytes a row, 16-byte piece
+// j of row r at position j ^ (r % 8): a quarter-warp's accesses fall in distinct banks),
+// then each store instruction writes four whole 128-byte row pieces.  Rows >= M and
+// columns >= ncols are not written.
+__device__ __forceinline__ void pair_emit(const float (&val)[32], float *chunk, long long ld,
+                                          int r0, int ncols, int M, float4 *stg, int lane) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        stg[lane * 8 + (j ^ (lane & 7))] =
+            make_float4(val[4 * j], val[4 * j + 1], val[4 * j + 2], val[4 * j + 3]);
+    __syncwarp();
+    const int cc = (lane & 7) * 4;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const int rr = 4 * t + (lane >> 3), gr = r0 + rr;
+        const float4 x = stg[rr * 8 + ((lane & 7) ^ (rr & 7))];
+        if (gr < M && cc < ncols) {
+            float *dst = chunk + (long long)gr * ld + cc;
+            if (cc + 4 <= ncols) {
+                *reinterpret_cast<float4 *>(dst) = x;
+            } else {
+                dst[0] = x.x;
+                if (cc + 1 < ncols) dst[1] = x.y;
+                if (cc + 2 < ncols) dst[2] = x.z;
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// Named barrier of epilogue warps 4 + q and 8 + q (literal ids 1..4), and the same
+// barrier returning whether v held in every thread of both warps (the pair leaves its
+// loop together, so that neither waits at the barrier for one that has left).
+__device__ __forceinline__ void pair_sync(int q) {
+    switch (q) {
+        case 0: named_barrier_sync(1, 64); break;
+        case 1: named_barrier_sync(2, 64); break;
+        case 2: named_barrier_sync(3, 64); break;
+        default: named_barrier_sync(4, 64); break;
+    }
+}
+__device__ __forceinline__ bool pair_and(int q, bool v) {
+    switch (q) {
+        case 0: return named_barrier_and(1, 64, v);
+        case 1: return named_barrier_and(2, 64, v);
+        case 2: return named_barrier_and(3, 64, v);
+        default: return named_barrier_and(4, 64, v);
+    }
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1) tc_pair_kernel(const GemmArgs g, int tiles_m,
+                                                                   long long tiles) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *img = base;                                   // Kbar hi, lo, Vbar hi, lo
+    uint8_t *ring = base + 4 * kPairImg;                   // Q hi, lo, dO hi, lo
+    float4 *stg_all = reinterpret_cast<float4 *>(ring + 4 * kPairTile);
+    uint64_t *a_full = reinterpret_cast<uint64_t *>(ring + 4 * kPairTile + 8 * kPairStg);  // [2]
+    uint64_t *a_empty = a_full + 2;    // [2]
+    uint64_t *b_full = a_empty + 2, *b_empty = b_full + 1;
+    uint64_t *acc_full = b_empty + 1, *acc_empty = acc_full + 1, *drain = acc_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // this CTA's row tiles [t0, t1): unit t / tiles_m, tile t % tiles_m
+    const long long t0 = tiles * blockIdx.x / gridDim.x, t1 = tiles * (blockIdx.x + 1) / gridDim.x;
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(a_full + i, kPairProducerWarps);
+            mbar_init(a_empty + i, 1);
+        }
+        mbar_init(b_full, kPairProducerWarps);
+        mbar_init(b_empty, 1);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kPairMmaWarp) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < kPairProducerWarps) {
+        // ---- producers: each unit's Kbar and Vbar once, each tile's Q and dO
+        int ub = 0, cur_z = -1;
+        bool ok = true;
+        for (long long t = t0; ok && t < t1; ++t) {
+            const int i = (int)(t - t0), z = (int)(t / tiles_m), mt = (int)(t % tiles_m);
+            if (z != cur_z) {
+                if (ub >= 1 && !warp_wait(b_empty, (ub - 1) & 1, g.status, 36, abort_flag)) break;
+                pair_load_rows(g.B.mat(z, g.h), g.B.ld, 0, 32, g.N, g.K, 0, false, img, img + kPairImg, tid);
+                pair_load_rows(g.B2.mat(z, g.h), g.B2.ld, 0, 32, g.N, g.K, 0, false, img + 2 * kPairImg,
+                               img + 3 * kPairImg, tid);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_full);
+                ++ub;
+                cur_z = z;
+            }
+            const int L = tc_unit_length(g.pad, z, g.h, g.n);
+#pragma unroll 1
+            for (int term = 0; term < 2; ++term) {
+                if (i >= 1 && !warp_wait(a_empty + term, (i - 1) & 1, g.status, 32, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const Operand o = term ? g.A2 : g.A;
+                uint8_t *st = ring + term * 2 * kPairTile;
+                pair_load_rows(o.mat(z, g.h), o.ld, mt * kTM, 16, g.M, g.K, L, o.mask_x != 0, st,
+                               st + kPairTile, tid);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(a_full + term);
+            }
+        }
+    } else if (warp < kPairMmaWarp) {
+        // ---- epilogue: warp (q, hc) owns rows 32 q .. of the tile and columns 128 hc ..
+        const int q = warp & 3, hc = (warp - kPairEpiWarp0) >> 2;
+        float4 *stg = stg_all + (warp - kPairEpiWarp0) * (kPairStg / 16);
+        const float *xchg = reinterpret_cast<const float *>(stg_all + ((warp - kPairEpiWarp0) ^ 4) * (kPairStg / 16));
+        float *mine = reinterpret_cast<float *>(stg);
+        const uint32_t lanes = (uint32_t)(q * 32) << 16;
+        const int cbeg = 128 * hc, nloc = max(0, min(128, g.N - cbeg));
+        const float a2 = g.alpha * kLog2e;
+        for (long long t = t0; t < t1; ++t) {
+            const int i = (int)(t - t0), z = (int)(t / tiles_m), mt = (int)(t % tiles_m);
+            bool ok = warp_wait(acc_full, i & 1, g.status, 33, abort_flag);
+            tc_fence_after();
+            if (!pair_and(q, ok && *abort_flag == 0)) break;
+            const int r0 = mt * kTM + q * 32, row = r0 + lane;
+            const bool live = row < tc_unit_length(g.pad, z, g.h, g.n);
+            const uint32_t ts = tmem + lanes + (uint32_t)cbeg, td = ts + 256u;
+            // pass 1: the row maximum of S over both column halves
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+            for (int c = 0; c < nloc; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(ts + (uint32_t)c, v);
+                const int nv = nloc - c;
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    if (nv >= 32 || e < nv) mx0 = fmaxf(mx0, __uint_as_float(v[e]));
+                    if (nv >= 32 || e + 1 < nv) mx1 = fmaxf(mx1, __uint_as_float(v[e + 1]));
+                }
+            }
+            mine[lane] = fmaxf(mx0, mx1);
+            pair_sync(q);
+            const float m = a2 * fmaxf(mine[lane], xchg[lane]);
+            // pass 2: e = 2^(a2 s - m), its sum and sum e dP, both halves
+            float l0 = 0.f, l1 = 0.f, D0 = 0.f, D1 = 0.f;
+            for (int c = 0; c < nloc; c += 32) {
+                uint32_t vs[32], vd[32];
+                tmem_ld32_async(ts + (uint32_t)c, vs);
+                tmem_ld32_async(td + (uint32_t)c, vd);
+                tmem_wait_ld(vs);
+                tie32(vd);
+                float e[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) e[j] = ex2_approx(fmaf(a2, __uint_as_float(vs[j]), -m));
+                if (nloc - c < 32) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j >= nloc - c) e[j] = 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    l0 += e[j];
+                    l1 += e[j + 1];
+                    D0 = fmaf(e[j], __uint_as_float(vd[j]), D0);
+                    D1 = fmaf(e[j + 1], __uint_as_float(vd[j + 1]), D1);
+                }
+            }
+            mine[32 + lane] = l0 + l1;
+            mine[64 + lane] = D0 + D1;
+            pair_sync(q);
+            const float inv = 1.f / (mine[32 + lane] + xchg[32 + lane]);
+            const float D = g.alpha2 * inv * (mine[64 + lane] + xchg[64 + lane]);
+            pair_sync(q);  // the partner has read these before the staging rows are reused
+            // pass 3: P and dS of the warp's columns (rows at or past the length: zeros)
+            float *outP = g.C + (long long)z * g.sC + cbeg, *outS = g.C2 + (long long)z * g.sC + cbeg;
+            for (int c = 0; c < nloc; c += 32) {
+                float val[32];
+                {
+                    uint32_t vs[32];
+                    tmem_ld32(ts + (uint32_t)c, vs);
+                    if (live) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            val[j] = ex2_approx(fmaf(a2, __uint_as_float(vs[j]), -m)) * inv;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) val[j] = 0.f;
+                    }
+                }
+                pair_emit(val, outP + c, g.ldc, r0, min(32, nloc - c), g.M, stg, lane);
+                uint32_t vd[32];
+                tmem_ld32(td + (uint32_t)c, vd);
+                if (live) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) val[j] *= fmaf(g.alpha2, __uint_as_float(vd[j]), -D);
+                }
+                pair_emit(val, outS + c, g.ldc, r0, min(32, nloc - c), g.M, stg, lane);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);  // one arrival per epilogue warp
+        }
+    } else if (lane == 0) {
+        // ---- MMA issuer: S = alpha Q Kbar^T into columns 0.., dP = dO Vbar^T into 256..
+        const int nmma = (g.N + 31) / 32 * 32;
+        const uint32_t idesc = idesc_f16(kTM, nmma, 1, 0, 0);
+        int ub = 0, cur_z = -1;
+        bool ok = true;
+        for (long long t = t0; ok && t < t1; ++t) {
+            const int i = (int)(t - t0), z = (int)(t / tiles_m);
+            if (z != cur_z) {
+                if (ub >= 1) mma_commit(b_empty);  // the previous unit's products release Kbar, Vbar
+                ok = mbar_wait(b_full, ub & 1, g.status, 35, abort_flag);
+                if (!ok) break;
+                ++ub;
+                cur_z = z;
+            }
+            if (i >= 1) ok = mbar_wait(acc_empty, (i - 1) & 1, g.status, 34, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int term = 0; term < 2; ++term) {
+                ok = mbar_wait(a_full + term, i & 1, g.status, 31, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t *st = ring + term * 2 * kPairTile, *bt = img + term * 2 * kPairImg;
+                const uint64_t ah = tile_desc(st, 0), al = tile_desc(st + kPairTile, 0);
+                const uint64_t bh = tile_desc(bt, 0), bl = tile_desc(bt + kPairImg, 0);
+                const uint32_t d = tmem + (uint32_t)(term * 256);
+#pragma unroll
+                for (int k = 0; k < kTK / 16; ++k) {
+                    mma_ss(d, ah + 2 * k, bh + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    mma_ss(d, ah + 2 * k, bl + 2 * k, idesc, 1u);
+                    mma_ss(d, al + 2 * k, bh + 2 * k, idesc, 1u);
+                }
+                mma_commit(a_empty + term);
+            }
+            if (!ok) break;
+            mma_commit(acc_full);
+        }
+        mma_commit(drain);
+        mbar_wait_drain(drain, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kPairMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+// Whether the pair kernel serves this kEpiSoftmaxPair product: d <= 64 (one 64-deep
+// step), K-major operands whose rows are 16-byte groups, outputs whose rows are too.
+bool pair_kernel_fits(const GemmArgs &g) {
+    auto kmajor_vec = [](const Operand &o) { return !o.xfast && o.vec && !o.mask_k; };
+    return g.K <= kTK && g.K % 4 == 0 && g.N % 4 == 0 && g.N <= 256 && kmajor_vec(g.A) &&
+           kmajor_vec(g.B) && kmajor_vec(g.A2) && kmajor_vec(g.B2) && !g.B.mask_x &&
+           !g.B2.mask_x && (reinterpret_cast<uintptr_t>(g.C) & 15) == 0 &&
+           (reinterpret_cast<uintptr_t>(g.C2) & 15) == 0 && g.ldc % 4 == 0 && g.sC % 4 == 0;
+}
+
+int launch_pair(const GemmArgs &g, int units, int sms, cudaStream_t s, int kernel_id) {
+    const int tiles_m = (g.M + kTM - 1) / kTM;
+    const long long tiles = (long long)tiles_m * units;
+    if (tiles <= 0) return LINFORMER_OK;
+    const long long grid = std::min<long long>(tiles, sms);
+    if (cudaFuncSetAttribute(tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPairSmem) != cudaSuccess)
+        return LINFORMER_ERR_LAUNCH;
+    {
+        KernelScope scope(kernel_id, s);
+        tc_pair_kernel<<<(unsigned)grid, kPairThreads, kPairSmem, s>>>(g, tiles_m, tiles);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
+}
+
 }  // namespace
 
 int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, size_t part_floats,
@@ -718,6 +1056,10 @@ int tc_batched_gemm(GemmArgs g, int units, cudaStream_t s, float *part, size_t p
             return LINFORMER_ERR_SIZE;
         set_operand_vec(g.A2, g.A2.xfast ? g.M : g.K);
         set_operand_vec(g.B2, g.B2.xfast ? g.N : g.K);
+        if (pair_kernel_fits(g)) {
+            g.status = device_status_ptr();
+            return launch_pair(g, units, sms, s, kernel_id);
+        }
     }
     Sched sc{};
     sc.tiles_m = (g.M + kTM - 1) / kTM;

@@ -227,7 +227,16 @@ __device__ __noinline__ void split_tiles_scan(const AttnParams &p, TileRanges *r
 // CTA).  Otherwise the weighted scan, kept out of line.
 __device__ __forceinline__ void split_tiles(const AttnParams &p, TileRanges *r, long long *scan) {
     const int U = p.units, G = gridDim.x, c = blockIdx.x, tpu = p.tiles_per_unit;
-    if (p.pad == nullptr && (p.forced_terms != 0 || __popc(__ldg(p.terms_seen)) == 1)) {
+    // One product count throughout: forced, or the same in every unit's info word
+    // (the whole CTA checks; every thread takes part in the vote).
+    bool uniform = p.forced_terms != 0;
+    if (p.pad == nullptr && !uniform) {
+        const int t0 = info_terms(__ldg(p.info));
+        int same = 1;
+        for (int u = threadIdx.x; u < U; u += blockDim.x) same &= info_terms(__ldg(p.info + u)) == t0;
+        uniform = __syncthreads_and(same) != 0;
+    }
+    if (p.pad == nullptr && uniform) {
         if (threadIdx.x == 0) {
             const long long X = (long long)U * tpu;
             long long b0, b1;
@@ -521,6 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Everything above overlaps the projection's last CTAs; its images and info
     // words are read only after this.
     wait_prerequisites();
+    // The next forward's projection may be scheduled on SMs as this grid's CTAs leave
+    // (it waits for the whole grid before it touches the workspace).
+    if (tid == 0) launch_dependents();
     split_tiles(p, ranges, reinterpret_cast<long long *>(rsum));  // rsum is free until the tiles
     tc_fence_before();
     __syncthreads();

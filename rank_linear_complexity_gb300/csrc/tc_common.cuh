@@ -175,7 +175,6 @@ struct ProjParams {
     int stages2;         // ring depth of those CTAs
     int prefetch;        // stages fetched into L2 ahead of the ring (0: none)
     int prefetch_proj;   // whether the E (and F) tiles are prefetched as well
-    int *terms_seen;     // bit t set if some unit takes t P.Vbar products (zero on entry)
 };
 
 struct AttnParams {
@@ -183,15 +182,14 @@ struct AttnParams {
     void *out;           // O, [units][n][64] bf16 or fp32: fully padded tiles are zeroed through it
     const uint8_t *images;
     const int *info;
-    const int *terms_seen;  // bit t set if some unit takes t P.Vbar products
     int *status;
     int h, n, k, kpad, units, tiles_per_unit, forced_terms, out_fp32;
     float scale_log2;    // log2(e) / sqrt(d)
 };
 
 // The host's plan of one tensor-core forward: the projection's launch and the
-// workspace layout (images, split partials, per-unit counters + the product-count
-// summary word, per-unit info words, each piece rounded up to 256 bytes).
+// workspace layout (images, split partials, per-unit counters, per-unit info words,
+// each piece rounded up to 256 bytes).
 struct ForwardPlan {
     ProjPlan proj;
     int64_t units, members, groups;

@@ -81,8 +81,8 @@ int plan_forward(const Problem &p, size_t part_budget, ForwardPlan *fp) {
     f.members = f.per_head ? p.b : f.units;
     f.groups = f.units / f.members;
     f.img = up256(f.units * 4 * image_bytes(f.kpad));
-    // per unit the split reduction's arrival counters, + the product-count summary word
-    f.cnt = up256((f.units * kCountersPerUnit + 1) * sizeof(int));
+    // per unit the split reduction's arrival counters
+    f.cnt = up256(f.units * kCountersPerUnit * sizeof(int));
     if (part_budget != ~size_t(0)) {  // a fixed workspace: images, counters and info first
         if (f.img + 2 * f.cnt > part_budget) return LINFORMER_ERR_SIZE;
         part_budget -= f.img + 2 * f.cnt;
@@ -105,9 +105,11 @@ int run_forward(const Problem &p, const ForwardPlan &f, char *ws, float *Kbar_ou
     float *partial = f.proj.C > 1 ? reinterpret_cast<float *>(ws + f.img) : nullptr;
     int *counters = reinterpret_cast<int *>(ws + f.img + f.part);
     int *info = reinterpret_cast<int *>(ws + f.img + f.part + f.cnt);
-    // Counters and the product-count summary start at zero (also when the workspace
-    // is reused from an earlier call).
-    if (cudaMemsetAsync(counters, 0, f.cnt, p.stream) != cudaSuccess) return LINFORMER_ERR_LAUNCH;
+    // The split reduction's counters start at zero (also when the workspace is reused
+    // from an earlier call); unsplit units use none, and then nothing comes between
+    // the previous kernel in the stream and the projection, which may start early.
+    if (f.proj.C > 1 && cudaMemsetAsync(counters, 0, f.cnt, p.stream) != cudaSuccess)
+        return LINFORMER_ERR_LAUNCH;
 
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t groups = (uint64_t)f.groups;
@@ -124,7 +126,6 @@ int run_forward(const Problem &p, const ForwardPlan &f, char *ws, float *Kbar_ou
     pp.partial = partial;
     pp.images = images;
     pp.counters = counters;
-    pp.terms_seen = counters + units * kCountersPerUnit;
     pp.info = info;
     pp.kbar_out = Kbar_out;
     pp.vbar_out = Vbar_out;
@@ -162,7 +163,6 @@ int run_forward(const Problem &p, const ForwardPlan &f, char *ws, float *Kbar_ou
     ap.out = p.O;
     ap.images = images;
     ap.info = info;
-    ap.terms_seen = counters + units * kCountersPerUnit;
     ap.status = status;
     ap.h = p.h;
     ap.n = p.n;

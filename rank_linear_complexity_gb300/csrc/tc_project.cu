@@ -71,8 +71,12 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // The attention kernel may take SMs as this grid's CTAs leave; it waits for the
-    // whole grid before it reads anything written here.
+    // Launched as a programmatic dependent of the previous kernel in the stream (the
+    // previous forward's attention, say, which reads this workspace): nothing is read
+    // or written before that grid has completed; only the launch overlaps its end.
+    // Then this forward's attention kernel may take SMs as this grid's CTAs leave; it
+    // waits for the whole grid before it reads anything written here.
+    wait_prerequisites();
     if (tid == 0) launch_dependents();
 
     // CTA -> (group g, chunk c, slot); members of a group share E (and F).  Slots
@@ -379,10 +383,7 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
                     flush(stg, img + 2 * image_bytes(p.kpad),
                           terms >= 2 ? img + 3 * image_bytes(p.kpad) : nullptr, mh, rows);
                 }
-                if (jl == 0) {
-                    p.info[uu] = pack_info(terms, e);
-                    atomicOr(p.terms_seen, 1 << terms);
-                }
+                if (jl == 0) p.info[uu] = pack_info(terms, e);
                 named_barrier_sync(1, 128);  // red[] is reused by the next unit
             }
         }
@@ -637,7 +638,6 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
         }
         if (tid == 0) {
             p.info[uu] = pack_info(terms, e);
-            atomicOr(p.terms_seen, 1 << terms);
             for (int i = 0; i < kCountersPerUnit; ++i) p.counters[(size_t)uu * kCountersPerUnit + i] = 0;
         }
         __syncthreads();  // red[] is reused by the next unit
@@ -673,10 +673,25 @@ int launch_project(const CUtensorMap &tE, const CUtensorMap &tF, const CUtensorM
         configured_dev = dev;
     }
     KernelScope scope(LINFORMER_KERNEL_PROJECT_TC, s);
-    if (p.kbar_out || p.vbar_out)
-        tc_project_kernel<true><<<grid, threads, smem, s>>>(tE, tF, tK, tV, p);
-    else
-        tc_project_kernel<false><<<grid, threads, smem, s>>>(tE, tF, tK, tV, p);
+    // Programmatic serialisation: the grid may be scheduled while the previous kernel in
+    // the stream finishes (the kernel waits for it before touching memory).
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = (p.kbar_out || p.vbar_out)
+                              ? cudaLaunchKernelEx(&cfg, tc_project_kernel<true>, tE, tF, tK, tV, p)
+                              : cudaLaunchKernelEx(&cfg, tc_project_kernel<false>, tE, tF, tK, tV, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return LINFORMER_ERR_LAUNCH;
+    }
     return cudaPeekAtLastError() == cudaSuccess ? LINFORMER_OK : LINFORMER_ERR_LAUNCH;
 }
 

@@ -224,6 +224,23 @@ def test_pv_products_match_oracle(terms, vscale):
     check(host64(O), ref, BF16, f"terms={terms} vscale={vscale}")
 
 
+@pytest.mark.parametrize("k", [1, 16, 40, 64, 100, 128, 200, 256])
+def test_three_products_at_every_key_layout(k):
+    """Three P.Vbar products forced where a key half has one, two, three or four chunks
+    (up to k_pad = 128 the tile keeps P_lo after its P in its own buffer, both chunks
+    read first; above, P_lo goes to the other buffer), with ragged lengths and a ragged
+    last query tile."""
+    b, h, n, d, mode = 2, 3, 1000, 64, PER_HEAD
+    x = case_inputs(b, h, n, d, k, mode, BF16, ragged=True, seed=44)
+    ref = oracle_full(x, mode)
+    prev = lf.linformer_set_pv_terms(3)
+    try:
+        O = run(x, mode, BF16)
+    finally:
+        lf.linformer_set_pv_terms(prev)
+    check(host64(O), ref, BF16, f"three products, k={k}")
+
+
 # --- scores that grow along the keys ---------------------------------------------------
 
 @pytest.mark.parametrize("mode", [PER_HEAD, HEADWISE])

@@ -184,3 +184,34 @@ def test_permuting_projected_positions_on_gpu(mode, dtype, k):
     ref = orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"], mode)[0]
     check(host64(outs[1]), ref, dtype, "permuted E/F against the unpermuted oracle")
     check(host64(outs[0]), ref, dtype, "unpermuted")
+
+
+# --- forwards one after another in a stream --------------------------------------------------
+
+def test_forwards_in_a_stream_see_inputs_written_between_them():
+    """The projection is launched as a programmatic dependent of whatever kernel precedes it
+    and waits for that grid before it reads or writes anything; the attention lets the
+    next kernel launch early.  A forward that follows PyTorch kernels rewriting Q, K, V and
+    E in place on the same stream must see the new values, and a forward launched right
+    after another (its projection overlapping the previous attention's last CTAs) must
+    give the same result.  Unsplit units, so no memset separates the launches."""
+    b, h, n, d, k, mode = 4, 12, 2048, 64, 256, LAYERWISE
+    x = case_inputs(b, h, n, d, k, mode, BF16, seed=77)
+    y = case_inputs(b, h, n, d, k, mode, BF16, seed=78)
+    g, gy = to_device(x, DEV), to_device(y, DEV)
+
+    def fwd():
+        return lf.attention(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], mode)
+
+    O1 = fwd()
+    for key in ("Q", "K", "V", "E"):  # elementwise kernels, not copies: 0 x + y == y exactly
+        g[key].mul_(0).add_(gy[key])
+    O2 = fwd()
+    O3 = fwd()
+    torch.cuda.synchronize()
+    assert lf.linformer_debug_read_device_status() == 0
+    check(host64(O1), orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                        mode)[0], BF16, "first forward")
+    ref_y = orc.linformer_fwd(y["Q"], y["K"], y["V"], y["E"], y["F"], y["lengths"], mode)[0]
+    check(host64(O2), ref_y, BF16, "forward after the inputs were rewritten")
+    assert torch.equal(O2, O3), "back-to-back forwards differ"

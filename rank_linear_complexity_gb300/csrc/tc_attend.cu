@@ -36,9 +36,7 @@
 //   P_a over S columns [0, c_b / 2), P_b over [c_b, c_b + (k_pad - c_b) / 2)
 //   O_a = P_a . Vbar_a at column 64 (128 when k_pad <= 128), O_b at column 192
 // Units whose |Vbar| is larger take two products for P . Vbar (P_hi . Vbar_lo
-// added) or, larger still, three (P_lo . Vbar_hi too).  With k_pad <= 128 a half has at
-// most two chunks, both read before anything is written, and P_lo takes the half's
-// columns after its P (scores already read); with k_pad > 128 P_lo sits in the other
+// added) or, larger still, three (P_lo . Vbar_hi too); P_lo then sits in the other
 // buffer at the same columns as P, so such a tile holds both buffers and runs alone.
 // The softmax is exact and two-pass (row max, then exp2 with the 1/sqrt(d)
 // scale folded in, row sum); scores never leave the SM.
@@ -116,7 +114,7 @@ __device__ __forceinline__ void unit_cost(const AttnParams &p, int u, int &live,
     const int L = valid_length(p.pad, u / p.h, p.n);
     live = (L + kTileM - 1) / kTileM;
     const int terms = p.forced_terms ? p.forced_terms : info_terms(__ldg(p.info + u));
-    weight = terms == 1 ? 10 : (terms == 2 ? 11 : (p.kpad <= 128 ? 13 : 19));
+    weight = terms == 1 ? 10 : (terms == 2 ? 11 : 19);
 }
 
 // A CTA's share of the work.  Live tiles (unit-major, then tile) are cut into
@@ -420,8 +418,7 @@ __device__ __forceinline__ void combine_halves(uint32_t *o, const uint32_t (&ob)
 // them to the row maximum.  Returns the half's row sum and (in mb) its maximum
 // in scaled log2 units.  TMEM loads run one chunk ahead of the arithmetic.
 __device__ __forceinline__ float softmax_half(uint32_t buf, uint32_t other, int c0, int nch,
-                                              int k, float scale, bool three, bool lo_here,
-                                              float &mb) {
+                                              int k, float scale, bool three, float &mb) {
     uint32_t va[32], vb[32];
     float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
     if (nch > 0) tmem_ld32_async(buf + c0, va);
@@ -441,21 +438,7 @@ __device__ __forceinline__ float softmax_half(uint32_t buf, uint32_t other, int 
     }
     mb = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * scale;
     float l0 = 0.f, l1 = 0.f;
-    if (three && nch > 0 && nch <= 2 && lo_here) {
-        // rare: P_lo of chunk c at column c0 + 16 (nch + c), over this half's scores,
-        // so both chunks are read first
-        tmem_ld32_async(buf + c0, va);
-        if (nch > 1) tmem_ld32_async(buf + c0 + 32, vb);
-        tmem_wait_ld(va);
-        if (nch > 1) tie32(vb);
-        const uint32_t lo = buf + c0 + 16 * nch;
-        if (c0 + 32 <= k) exp_chunk3<false>(va, buf + c0, lo, c0, k, scale, mb, l0, l1);
-        else exp_chunk3<true>(va, buf + c0, lo, c0, k, scale, mb, l0, l1);
-        if (nch > 1) {
-            if (c0 + 64 <= k) exp_chunk3<false>(vb, buf + c0 + 16, lo + 16, c0 + 32, k, scale, mb, l0, l1);
-            else exp_chunk3<true>(vb, buf + c0 + 16, lo + 16, c0 + 32, k, scale, mb, l0, l1);
-        }
-    } else if (three) {  // rare; one chunk in registers at a time, P_lo in the other buffer
+    if (three) {  // rare; one chunk in registers at a time
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
             const int ca = c0 + 32 * c;
@@ -517,7 +500,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t img_bytes = (uint32_t)p.kpad * kRowBytes;
     const KeySplit ks = key_split(p.k, p.kpad);
-    const bool lo_here = p.kpad <= 128;  // three products keep P_lo in the tile's own buffer
 
     if (tid == 0) {
         mbar_init(k_full, 1);
@@ -612,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t uw = w ? uses1 : uses0, uo = w ? uses0 : uses1;
                     if (uw > 0 && !mbar_wait(tmem_free + w, (uw - 1) & 1, p.status, 24, abort_flag))
                         break;
-                    if (terms == 3 && !lo_here && uo > 0 &&
+                    if (terms == 3 && uo > 0 &&
                         !mbar_wait(tmem_free + (w ^ 1), (uo - 1) & 1, p.status, 24, abort_flag))
                         break;
                     if (!mbar_wait(q_full + slot, (j / kQSlots) & 1, p.status, 25, abort_flag)) break;
@@ -628,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(q_empty + slot);
                     if (w) ++uses1;
                     else ++uses0;
-                    if (terms == 3 && !lo_here) {
+                    if (terms == 3) {
                         if (w) ++uses0;
                         else ++uses1;
                     }
@@ -679,9 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t a = tmem + kBufCols * w + c0;          // P_half: 8 columns per step
-                    // P_lo (three products): after the half's P, or in the other buffer
-                    const uint32_t alo = lo_here ? tmem + kBufCols * w + c0 + 16 * (h ? ks.n1 : ks.n0)
-                                                 : tmem + kBufCols * (w ^ 1) + c0;
+                    const uint32_t alo = tmem + kBufCols * (w ^ 1) + c0;  // P_lo half (three products)
                     const uint32_t dO = tmem + kBufCols * w + ocol;
     #pragma unroll
                     for (int s = 0; s < 8; ++s)  // at most 8 steps of 16 keys per half
@@ -764,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(tmem_free + w);
-                        if (wk.terms == 3 && !lo_here) mbar_arrive(tmem_free + (w ^ 1));
+                        if (wk.terms == 3) mbar_arrive(tmem_free + (w ^ 1));
                     }
                 }
             }
@@ -836,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float mb;
             const float l = softmax_half(tmem + lane_off + kBufCols * w,
                                          tmem + lane_off + kBufCols * (w ^ 1), c0, nch, p.k,
-                                         p.scale_log2, wk.terms == 3, p.kpad <= 128, mb);
+                                         p.scale_log2, wk.terms == 3, mb);
             rsum[(w * 2 + h) * kTileM + tw] = l;
             rmax[(w * 2 + h) * kTileM + tw] = mb;
             tc_fence_before();

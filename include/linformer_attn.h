@@ -44,7 +44,14 @@
  * which keeps freed memory mapped for the next call until the process exits (as much
  * as the largest call in flight needed).  Calls are asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream): inputs must stay unchanged until the stream has
- * passed the call.  Calls on different streams may run concurrently.
+ * passed the call.  Calls on different streams may run concurrently.  The forward's
+ * first kernel is launched with programmatic stream serialisation and waits for the
+ * kernel before it (griddepcontrol.wait) before it reads or writes memory; its last
+ * kernel lets the next kernel in the stream launch early, so a caller's kernel that
+ * is itself launched with programmatic stream serialisation after a call must wait
+ * for its prerequisite grid (cudaGridDependencySynchronize) before it reads O, as
+ * CUDA requires of any such kernel.  Kernels launched without that attribute are
+ * ordered as usual.
  *
  * Errors: every function returns LINFORMER_OK (0) or a negative status; no call
  * traps or aborts.  Argument errors are detected on the host before anything is

@@ -215,3 +215,41 @@ def test_forwards_in_a_stream_see_inputs_written_between_them():
     ref_y = orc.linformer_fwd(y["Q"], y["K"], y["V"], y["E"], y["F"], y["lengths"], mode)[0]
     check(host64(O2), ref_y, BF16, "forward after the inputs were rewritten")
     assert torch.equal(O2, O3), "back-to-back forwards differ"
+
+
+def test_two_streams_and_the_projection_entry_point_interleaved():
+    """Forwards on two streams at once (each stream's projection waits only for its own
+    stream's previous kernel), and the projection-only entry point between forwards in
+    one stream: every result against the oracle."""
+    b, h, n, d, k, mode = 2, 12, 2048, 64, 256, PER_HEAD
+    xs = [case_inputs(b, h, n, d, k, mode, BF16, seed=80 + i) for i in range(2)]
+    gs = [to_device(x, DEV) for x in xs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = [[], []]
+    for _ in range(3):
+        for i in (0, 1):
+            g = gs[i]
+            with torch.cuda.stream(streams[i]):
+                outs[i].append(lf.attention(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"],
+                                            mode, stream=streams[i].cuda_stream))
+    with torch.cuda.stream(streams[0]):
+        g = gs[0]
+        kb, vb = lf.projection(g["K"], g["V"], g["E"], g["F"], g["lengths"], mode,
+                               stream=streams[0].cuda_stream)
+        outs[0].append(lf.attention(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], mode,
+                                    stream=streams[0].cuda_stream))
+    torch.cuda.synchronize()
+    assert lf.linformer_debug_read_device_status() == 0
+    for i in (0, 1):
+        x = xs[i]
+        ref, _, rK, rV = orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                           mode, return_proj=True)
+        for j, O in enumerate(outs[i]):
+            check(host64(O), ref, BF16, f"stream {i}, call {j}")
+            assert torch.equal(O, outs[i][0]), f"stream {i}: call {j} differs from call 0"
+        if i == 0:
+            for got, want in ((kb, rK), (vb, rV)):
+                w = np.asarray(want, np.float64)
+                err = np.abs(host64(got) - w).max()
+                assert err <= 1e-4 * max(np.abs(w).max(), 1e-30), err

@@ -36,8 +36,12 @@
 //   P_a over S columns [0, c_b / 2), P_b over [c_b, c_b + (k_pad - c_b) / 2)
 //   O_a = P_a . Vbar_a at column 64 (128 when k_pad <= 128), O_b at column 192
 // Units whose |Vbar| is larger take two products for P . Vbar (P_hi . Vbar_lo
-// added) or, larger still, three (P_lo . Vbar_hi too); P_lo then sits in the other
-// buffer at the same columns as P, so such a tile holds both buffers and runs alone.
+// added) or, larger still, three (P_lo . Vbar_hi too).  With k_pad > 128 P_lo sits in
+// the other buffer at the same columns as P, so such a tile holds both buffers and runs
+// alone.  With k_pad <= 128 (a separate instantiation, kLoHere: its code would otherwise
+// change the register allocation of the common path of the k_pad > 128 one) a half has
+// at most two chunks, both read before anything is written, and P_lo follows the half's
+// P over its own scores, so such a tile keeps one buffer and the double buffering.
 // The softmax is exact and two-pass (row max, then exp2 with the 1/sqrt(d)
 // scale folded in, row sum); scores never leave the SM.
 #include <cuda_bf16.h>
@@ -109,12 +113,13 @@ __device__ __forceinline__ KeySplit key_split(int k, int kpad) {
 }
 
 // Query tiles of a unit that hold at least one valid row, and the relative cost
-// of one such tile (by the number of P.Vbar products: measured about 1 : 1.1 : 1.9).
+// of one such tile (by the number of P.Vbar products: measured about 1 : 1.1 : 1.9, and
+// 1.3 for three products with k_pad <= 128, where such a tile keeps the double buffering).
 __device__ __forceinline__ void unit_cost(const AttnParams &p, int u, int &live, int &weight) {
     const int L = valid_length(p.pad, u / p.h, p.n);
     live = (L + kTileM - 1) / kTileM;
     const int terms = p.forced_terms ? p.forced_terms : info_terms(__ldg(p.info + u));
-    weight = terms == 1 ? 10 : (terms == 2 ? 11 : 19);
+    weight = terms == 1 ? 10 : (terms == 2 ? 11 : (p.kpad <= 128 ? 13 : 19));
 }
 
 // A CTA's share of the work.  Live tiles (unit-major, then tile) are cut into
@@ -417,6 +422,7 @@ __device__ __forceinline__ void combine_halves(uint32_t *o, const uint32_t (&ob)
 // that the two halves of a row never wait for each other; the epilogue brings
 // them to the row maximum.  Returns the half's row sum and (in mb) its maximum
 // in scaled log2 units.  TMEM loads run one chunk ahead of the arithmetic.
+template <bool kLoHere>
 __device__ __forceinline__ float softmax_half(uint32_t buf, uint32_t other, int c0, int nch,
                                               int k, float scale, bool three, float &mb) {
     uint32_t va[32], vb[32];
@@ -438,16 +444,27 @@ __device__ __forceinline__ float softmax_half(uint32_t buf, uint32_t other, int 
     }
     mb = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * scale;
     float l0 = 0.f, l1 = 0.f;
-    if (three) {  // rare; one chunk in registers at a time
+    if (three) {
+        // rare; one chunk in registers at a time.  P_lo goes to the other buffer, or with
+        // kLoHere (k_pad <= 128: at most two chunks) after this half's P, over scores that
+        // must be read first: the second chunk is loaded with the first and moved over.
+        if (kLoHere && nch > 1) tmem_ld32_async(buf + c0 + 32, vb);
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
             const int ca = c0 + 32 * c;
-            tmem_ld32_async(buf + ca, va);
+            if (kLoHere && c == 1) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) va[i] = vb[i];
+            } else {
+                tmem_ld32_async(buf + ca, va);
+            }
             tmem_wait_ld(va);
+            if (kLoHere && nch > 1 && c == 0) tie32(vb);
+            const uint32_t lcol = kLoHere ? buf + c0 + 16 * (nch + c) : other + c0 + 16 * c;
             if (ca + 32 <= k)
-                exp_chunk3<false>(va, buf + c0 + 16 * c, other + c0 + 16 * c, ca, k, scale, mb, l0, l1);
+                exp_chunk3<false>(va, buf + c0 + 16 * c, lcol, ca, k, scale, mb, l0, l1);
             else
-                exp_chunk3<true>(va, buf + c0 + 16 * c, other + c0 + 16 * c, ca, k, scale, mb, l0, l1);
+                exp_chunk3<true>(va, buf + c0 + 16 * c, lcol, ca, k, scale, mb, l0, l1);
         }
     } else {
         if (nch > 0) tmem_ld32_async(buf + c0, va);
@@ -472,6 +489,7 @@ __device__ __forceinline__ float softmax_half(uint32_t buf, uint32_t other, int 
     return l0 + l1;
 }
 
+template <bool kLoHere>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_attend_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tO,
                      const AttnParams p) {
@@ -594,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t uw = w ? uses1 : uses0, uo = w ? uses0 : uses1;
                     if (uw > 0 && !mbar_wait(tmem_free + w, (uw - 1) & 1, p.status, 24, abort_flag))
                         break;
-                    if (terms == 3 && uo > 0 &&
+                    if (terms == 3 && !kLoHere && uo > 0 &&
                         !mbar_wait(tmem_free + (w ^ 1), (uo - 1) & 1, p.status, 24, abort_flag))
                         break;
                     if (!mbar_wait(q_full + slot, (j / kQSlots) & 1, p.status, 25, abort_flag)) break;
@@ -610,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(q_empty + slot);
                     if (w) ++uses1;
                     else ++uses0;
-                    if (terms == 3) {
+                    if (terms == 3 && !kLoHere) {
                         if (w) ++uses0;
                         else ++uses1;
                     }
@@ -661,7 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t a = tmem + kBufCols * w + c0;          // P_half: 8 columns per step
-                    const uint32_t alo = tmem + kBufCols * (w ^ 1) + c0;  // P_lo half (three products)
+                    // P_lo (three products): after the half's P, or in the other buffer
+                    const uint32_t alo = kLoHere ? tmem + kBufCols * w + c0 + 16 * (h ? ks.n1 : ks.n0)
+                                                 : tmem + kBufCols * (w ^ 1) + c0;
                     const uint32_t dO = tmem + kBufCols * w + ocol;
                     // At most 8 steps of 16 keys per half; the issue rate of one thread, not
                     // the loop, bounds these (rolled loops: smaller code, measured faster).
@@ -747,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(tmem_free + w);
-                        if (wk.terms == 3) mbar_arrive(tmem_free + (w ^ 1));
+                        if (wk.terms == 3 && !kLoHere) mbar_arrive(tmem_free + (w ^ 1));
                     }
                 }
             }
@@ -817,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (!ok) break;
             float mb;
-            const float l = softmax_half(tmem + lane_off + kBufCols * w,
+            const float l = softmax_half<kLoHere>(tmem + lane_off + kBufCols * w,
                                          tmem + lane_off + kBufCols * (w ^ 1), c0, nch, p.k,
                                          p.scale_log2, wk.terms == 3, mb);
             rsum[(w * 2 + h) * kTileM + tw] = l;
@@ -847,7 +867,9 @@ int launch_attend(const CUtensorMap &tQ, const CUtensorMap &tO, const AttnParams
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        if (cudaFuncSetAttribute(tc_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(tc_attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attend_smem_bytes(1)) != cudaSuccess ||
+            cudaFuncSetAttribute(tc_attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)attend_smem_bytes(1)) != cudaSuccess)
             return LINFORMER_ERR_LAUNCH;
         configured_dev = dev;
@@ -865,7 +887,10 @@ int launch_attend(const CUtensorMap &tQ, const CUtensorMap &tO, const AttnParams
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, tc_attend_kernel, tQ, tO, p) != cudaSuccess) {
+    // k_pad <= 128: the instantiation that keeps three-product tiles in one buffer.
+    const cudaError_t e = p.kpad <= 128 ? cudaLaunchKernelEx(&cfg, tc_attend_kernel<true>, tQ, tO, p)
+                                        : cudaLaunchKernelEx(&cfg, tc_attend_kernel<false>, tQ, tO, p);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return LINFORMER_ERR_LAUNCH;
     }

@@ -113,13 +113,16 @@ __device__ __forceinline__ KeySplit key_split(int k, int kpad) {
 }
 
 // Query tiles of a unit that hold at least one valid row, and the relative cost
-// of one such tile (by the number of P.Vbar products: measured about 1 : 1.1 : 1.9, and
-// 1.3 for three products with k_pad <= 128, where such a tile keeps the double buffering).
+// of one such tile (by the number of P.Vbar products: measured about 1 : 1.1 : 1.9 in
+// launches of one count, but a three-product tile with k_pad > 128, which holds both
+// buffers, costs about 2.5 among tiles of other counts (the ragged per-head workload:
+// 397.8 -> 374.5 us per forward with 25 instead of 19); 1.3 with k_pad <= 128, where such
+// a tile keeps the double buffering).  Only mixed launches use the weights.
 __device__ __forceinline__ void unit_cost(const AttnParams &p, int u, int &live, int &weight) {
     const int L = valid_length(p.pad, u / p.h, p.n);
     live = (L + kTileM - 1) / kTileM;
     const int terms = p.forced_terms ? p.forced_terms : info_terms(__ldg(p.info + u));
-    weight = terms == 1 ? 10 : (terms == 2 ? 11 : (p.kpad <= 128 ? 13 : 19));
+    weight = terms == 1 ? 10 : (terms == 2 ? 11 : (p.kpad <= 128 ? 13 : 25));
 }
 
 // A CTA's share of the work.  Live tiles (unit-major, then tile) are cut into

@@ -71,14 +71,6 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // Launched as a programmatic dependent of the previous kernel in the stream (the
-    // previous forward's attention, say, which reads this workspace): nothing is read
-    // or written before that grid has completed; only the launch overlaps its end.
-    // Then this forward's attention kernel may take SMs as this grid's CTAs leave; it
-    // waits for the whole grid before it reads anything written here.
-    wait_prerequisites();
-    if (tid == 0) launch_dependents();
-
     // CTA -> (group g, chunk c, slot); members of a group share E (and F).  Slots
     // below p.pairs take members 2 slot and 2 slot + 1 (one E tile per stage for
     // both; only unsplit units, E = F, no lengths), the others one member each.
@@ -93,13 +85,39 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
     const int u = p.per_head ? m * p.h + g : m;
     // the second unit of a pair (the next member of the same group)
     const int u_b = p.per_head ? (m + 1) * p.h + g : m + 1;
+    const int gproj = p.per_head ? g : 0;
+
+    // Launched as a programmatic dependent of the previous kernel in the stream (the
+    // previous forward's attention, say, which reads this workspace): nothing is read
+    // or written before that grid has completed.  Only L2 prefetches of this CTA's
+    // first stages of K, V and E go out before the wait, as if every row were valid
+    // (the lengths may not be read yet): a prefetch reads nothing into the CTA, and L2
+    // is where every write lands, so what the main loop later reads cannot be stale.
+    // Then this forward's attention kernel may take SMs as this grid's CTAs leave; it
+    // waits for the whole grid before it reads anything written here.
+    if (tid == 0) {
+        const int early = (nunits == 2 ? p.stages2 : p.stages) + p.prefetch;
+        const int nmax = (min(p.CH, p.n - c * p.CH) + kBK - 1) / kBK;
+        for (int j = 0; j < early && j < nmax; ++j) {
+            const int x = c * p.CH + j * kBK;
+            tma_prefetch_3d(&tK, 0, x, u);
+            tma_prefetch_3d(&tV, 0, x, u);
+            if (nunits == 2) {
+                tma_prefetch_3d(&tK, 0, x, u_b);
+                tma_prefetch_3d(&tV, 0, x, u_b);
+            }
+            tma_prefetch_3d(&tE, x, 0, gproj);
+            if (p.distinct) tma_prefetch_3d(&tF, x, 0, gproj);
+        }
+    }
+    wait_prerequisites();
+    if (tid == 0) launch_dependents();
     const int L = valid_length(p.pad, u / p.h, p.n);
     const int Cu = L > 0 ? (L + p.CH - 1) / p.CH : 1;
     if (c >= Cu) return;  // chunk entirely in the padding: nothing to add
     const int row0 = c * p.CH;
     const int rows = max(0, min(p.CH, L - row0));
     const int nkb = (rows + kBK - 1) / kBK;
-    const int gproj = p.per_head ? g : 0;
 
     // Stage: the E (and F) tile, then K and V tiles of 8 KB per unit, in the order
     // K_0 V_0 K_1 V_1 (one operand of 64-column atoms 8 KB apart).

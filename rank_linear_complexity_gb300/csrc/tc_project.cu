@@ -96,7 +96,11 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
     // Then this forward's attention kernel may take SMs as this grid's CTAs leave; it
     // waits for the whole grid before it reads anything written here.
     if (tid == 0) {
-        const int early = (nunits == 2 ? p.stages2 : p.stages) + p.prefetch;
+        // the ring, the main loop's own prefetch distance and, without lengths, four more
+        // (measured at the headline: 0, 6, 10, 16, 24 stages gave 148.0, 145.2, 144.2,
+        // 145.0, 147.6 us; with lengths the rows may be padding, and the ragged per-head
+        // workload took 373.6 us with the first two terms and 379.0 with four more)
+        const int early = (nunits == 2 ? p.stages2 : p.stages) + p.prefetch + (p.pad ? 0 : 4);
         const int nmax = (min(p.CH, p.n - c * p.CH) + kBK - 1) / kBK;
         for (int j = 0; j < early && j < nmax; ++j) {
             const int x = c * p.CH + j * kBK;

@@ -253,3 +253,44 @@ def test_two_streams_and_the_projection_entry_point_interleaved():
                 w = np.asarray(want, np.float64)
                 err = np.abs(host64(got) - w).max()
                 assert err <= 1e-4 * max(np.abs(w).max(), 1e-30), err
+
+
+@pytest.mark.parametrize("mode,k", [(LAYERWISE, 256), (PER_HEAD, 128)])
+@pytest.mark.parametrize("entry", ["linformer_attn_fwd", "linformer_attn_fwd_noalloc"])
+def test_forward_captured_in_a_cuda_graph(entry, mode, k):
+    """A forward captured in a CUDA graph (its stream-ordered workspace, its programmatic
+    launches) replays to the eager result bitwise, and sees inputs rewritten in place
+    between replays; checked against the oracle too.  Both attention instantiations
+    (k_pad > 128 and <= 128)."""
+    fn = getattr(lf, entry)
+    b, h, n, d = 2, 3, 1024, 64
+    x = case_inputs(b, h, n, d, k, mode, BF16, seed=95)
+    y = case_inputs(b, h, n, d, k, mode, BF16, seed=96)
+    g, gy = to_device(x, DEV), to_device(y, DEV)
+
+    def args(O, s):
+        return (g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], O, b, h, n, d, k, mode,
+                BF16, s)
+
+    O_eager = torch.empty_like(g["Q"])
+    assert fn(*args(O_eager, torch.cuda.current_stream().cuda_stream)) == 0  # first use: set-up
+    torch.cuda.synchronize()
+    O = torch.zeros_like(g["Q"])
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        assert fn(*args(O, s.cuda_stream)) == 0
+    graph.replay()
+    torch.cuda.synchronize()
+    assert lf.linformer_debug_read_device_status() == 0
+    assert torch.equal(O, O_eager)
+    check(host64(O), orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                       mode)[0], BF16, f"{entry} replay")
+    for key in ("Q", "K", "V", "E", "F"):
+        if g[key] is not None:
+            g[key].copy_(gy[key])
+    graph.replay()
+    torch.cuda.synchronize()
+    assert lf.linformer_debug_read_device_status() == 0
+    check(host64(O), orc.linformer_fwd(y["Q"], y["K"], y["V"], y["E"], y["F"], y["lengths"],
+                                       mode)[0], BF16, f"{entry} replay after new inputs")

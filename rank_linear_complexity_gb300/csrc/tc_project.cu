@@ -334,17 +334,20 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
 #pragma unroll 1
                 for (int mh = 0; mh < p.mhalves; ++mh) {
                     const int rows = min(128, p.kpad - 128 * mh);
-                    uint32_t v[64];
-                    tmem_ld64(lane_base + mh * 128 * nunits + ucol, v);
                     uint8_t *stg = claim();
-                    if (jl < rows) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
+                    // Rolled, 8 columns a step: this code runs once per unit, on every SM
+                    // at once and from a cold instruction cache, so its length costs more
+                    // than the eight short TMEM round trips.
+#pragma unroll 1
+                    for (int q = 0; q < 8; ++q) {
+                        uint32_t v[8];
+                        tmem_ld8(lane_base + mh * 128 * nunits + ucol + 8 * q, v);
+                        if (jl < rows) {
                             uint32_t hi[4], lo[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float x0 = __uint_as_float(v[q * 8 + 2 * e]);
-                                const float x1 = __uint_as_float(v[q * 8 + 2 * e + 1]);
+                                const float x0 = __uint_as_float(v[2 * e]);
+                                const float x1 = __uint_as_float(v[2 * e + 1]);
                                 const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
                                 const float2 hf = __bfloat1622float2(h);  // exact
                                 hi[e] = *reinterpret_cast<const uint32_t *>(&h);
@@ -380,17 +383,17 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
 #pragma unroll 1
                 for (int mh = 0; mh < p.mhalves; ++mh) {
                     const int rows = min(128, p.kpad - 128 * mh);
-                    uint32_t v[64];
-                    tmem_ld64(lane_base + mh * 128 * nunits + ucol + 64, v);
                     uint8_t *stg = claim();
-                    if (jl < rows) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
+#pragma unroll 1
+                    for (int q = 0; q < 8; ++q) {  // rolled, as for Kbar
+                        uint32_t v[8];
+                        tmem_ld8(lane_base + mh * 128 * nunits + ucol + 64 + 8 * q, v);
+                        if (jl < rows) {
                             uint32_t hi[4], lo[4];
 #pragma unroll
                             for (int e2 = 0; e2 < 4; ++e2) {
-                                const float x0 = __uint_as_float(v[q * 8 + 2 * e2]) * vscale;
-                                const float x1 = __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale;
+                                const float x0 = __uint_as_float(v[2 * e2]) * vscale;
+                                const float x1 = __uint_as_float(v[2 * e2 + 1]) * vscale;
                                 const __half2 h = __floats2half2_rn(x0, x1);
                                 const float2 hf = __half22float2(h);  // exact
                                 hi[e2] = *reinterpret_cast<const uint32_t *>(&h);
@@ -575,17 +578,20 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
 #pragma unroll 1
         for (int mh = 0; mh < p.mhalves; ++mh) {
             const int j = mh * 128 + jl;
-            uint32_t v[64];
-            tmem_ld64(lane_base + mh * 128 * nunits + ucol, v);
             uint8_t *stg = stage_claim();
-            if (j < p.kpad) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
+            // Rolled, 8 columns a step: this code runs once per unit, on every SM at once
+            // and from a cold instruction cache, so its length costs more than the eight
+            // short TMEM round trips.
+#pragma unroll 1
+            for (int q = 0; q < 8; ++q) {
+                uint32_t v[8];
+                tmem_ld8(lane_base + mh * 128 * nunits + ucol + 8 * q, v);
+                if (j < p.kpad) {
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float x0 = j < p.k ? __uint_as_float(v[q * 8 + 2 * e]) : 0.f;
-                        const float x1 = j < p.k ? __uint_as_float(v[q * 8 + 2 * e + 1]) : 0.f;
+                        const float x0 = j < p.k ? __uint_as_float(v[2 * e]) : 0.f;
+                        const float x1 = j < p.k ? __uint_as_float(v[2 * e + 1]) : 0.f;
                         const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
                         const float2 hf = __bfloat1622float2(h);  // exact
                         const float r0 = x0 - hf.x, r1 = x1 - hf.y;
@@ -627,17 +633,17 @@ __global__ void __launch_bounds__(2 * kThreads, 1)
 #pragma unroll 1
         for (int mh = 0; mh < p.mhalves; ++mh) {
             const int j = mh * 128 + jl;
-            uint32_t v[64];
-            tmem_ld64(lane_base + mh * 128 * nunits + ucol + 64, v);
             uint8_t *stg = stage_claim();
-            if (j < p.kpad) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
+#pragma unroll 1
+            for (int q = 0; q < 8; ++q) {  // rolled, as for Kbar
+                uint32_t v[8];
+                tmem_ld8(lane_base + mh * 128 * nunits + ucol + 64 + 8 * q, v);
+                if (j < p.kpad) {
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2) {
-                        const float x0 = j < p.k ? __uint_as_float(v[q * 8 + 2 * e2]) * vscale : 0.f;
-                        const float x1 = j < p.k ? __uint_as_float(v[q * 8 + 2 * e2 + 1]) * vscale : 0.f;
+                        const float x0 = j < p.k ? __uint_as_float(v[2 * e2]) * vscale : 0.f;
+                        const float x1 = j < p.k ? __uint_as_float(v[2 * e2 + 1]) * vscale : 0.f;
                         const __half2 h = __floats2half2_rn(x0, x1);
                         const float2 hf = __half22float2(h);  // exact
                         const float r0 = x0 - hf.x, r1 = x1 - hf.y;

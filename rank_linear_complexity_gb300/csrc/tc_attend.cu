@@ -581,7 +581,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int cur = -1, nk = 0, qit = 0;
                 for (TileWalk wk(p, rg); wk.more(); wk.next(p)) {
                     const int u = wk.u, t = wk.t;
-                    if (u != cur) {  // Kbar of the unit, once its predecessor's scores are done
+                    // The Q tile first (from HBM, the longer wait), then, on a change of
+                    // unit, the unit's Kbar images (from L2), once its predecessor's score
+                    // products are done.
+                    const int s = qit % kQSlots;
+                    if (qit >= kQSlots &&
+                        !mbar_wait(q_empty + s, ((qit / kQSlots) - 1) & 1, p.status, 22, abort_flag))
+                        break;
+                    mbar_arrive_expect_tx(q_full + s, kQBytes);
+                    tma_load_3d(sQ + s * kQBytes, &tQ, q_full + s, 0, t * kTileM, u);
+                    ++qit;
+                    if (u != cur) {
                         if (nk > 0 && !mbar_wait(k_empty, (nk - 1) & 1, p.status, 21, abort_flag))
                             break;
                         const uint8_t *src = p.images + (size_t)u * 4 * img_bytes;
@@ -591,13 +601,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++nk;
                         cur = u;
                     }
-                    const int s = qit % kQSlots;
-                    if (qit >= kQSlots &&
-                        !mbar_wait(q_empty + s, ((qit / kQSlots) - 1) & 1, p.status, 22, abort_flag))
-                        break;
-                    mbar_arrive_expect_tx(q_full + s, kQBytes);
-                    tma_load_3d(sQ + s * kQBytes, &tQ, q_full + s, 0, t * kTileM, u);
-                    ++qit;
                 }
                 // Let every copy this thread started land before the CTA may exit
                 // (also after an abort: a copy must not outlive the CTA).

@@ -551,8 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // L2 prefetches of the first query tiles of this CTA's range as the closed-form
     // partition gives it (a hint: a prefetch reads nothing into the CTA and cannot be
     // stale; useless only if the weighted partition applies).  Only in the k_pad <= 128
-    // instantiation: RoBERTa shape 50.1 -> 48.2 us per forward; in the other one the
-    // added code moved the common path's register allocation (headline 143.5 -> 145.2).
+    // instantiation: RoBERTa shape 50.1 -> 48.2 us per forward; the other one is slower
+    // with it (headline 143.0 -> 144.1 us), with the same registers and spills.
     if (kLoHere && tid == 0 && p.pad == nullptr) {
         const long long X = (long long)p.units * p.tiles_per_unit;
         const long long q = X / gridDim.x, r = X - q * gridDim.x;

@@ -69,6 +69,11 @@ constexpr uint32_t kImg = 32768;    // largest image: 256 rows x 128 bytes
 constexpr uint32_t kQBytes = 16384;
 constexpr int kQSlots = 3;
 constexpr uint32_t kPiece = 16384;  // one staged store: 128 rows x 128 bytes
+// Slots of the per-row maxima and sums: with k_pad <= 128 a tile's scores leave its
+// buffer's O columns alone, so the next score products into the buffer wait only for
+// the previous tile's P.V, and its softmax may end before that tile's epilogue has read
+// the row sums: they rotate over four slots by tile; with k_pad > 128 one per buffer.
+constexpr int kRowSlots = 4;
 constexpr uint32_t kEpilogueBarrier = 1;
 
 __device__ __forceinline__ int valid_length(const int32_t *pad, int batch, int n) {
@@ -502,9 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sKh = smem, *sKl = smem + kImg, *sVh = smem + 2 * kImg, *sVl = smem + 3 * kImg;
     uint8_t *sQ = smem + 4 * kImg;          // kQSlots x 16 KB
     uint8_t *sO = sQ + kQSlots * kQBytes;   // two 16 KB staging pieces
-    float *rmax = reinterpret_cast<float *>(sO + 2 * kPiece);  // [buffer][half][row]
-    float *rsum = rmax + 2 * 2 * kTileM;                       // [buffer][half][row]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(rsum + 2 * 2 * kTileM);
+    float *rmax = reinterpret_cast<float *>(sO + 2 * kPiece);  // [slot][half][row]
+    float *rsum = rmax + kRowSlots * 2 * kTileM;               // [slot][half][row]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rsum + kRowSlots * 2 * kTileM);
     uint64_t *k_full = bars + 0, *k_empty = bars + 1, *v_full = bars + 2, *v_empty = bars + 3;
     uint64_t *q_full = bars + 4, *q_empty = bars + 4 + kQSlots;
     uint64_t *s_full = bars + 4 + 2 * kQSlots;
@@ -517,6 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lets the thread wait for its own products before the CTA frees TMEM, also when
     // a wait elsewhere gave up.
     uint64_t *drain = s_full + 15;
+    // k_pad <= 128: one per row slot, completed by the eight softmax warps once the tile's
+    // row maxima and sums are written (the epilogue's signal; p_full may by then have run
+    // a phase ahead, its next tile in the buffer no longer waiting for the epilogue).
+    uint64_t *rows_ready = drain + 3;
+    static_assert(4 + 2 * kQSlots + 15 + 3 + kRowSlots <= 32, "barrier area");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t img_bytes = (uint32_t)p.kpad * kRowBytes;
@@ -539,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tmem_free + s, 4);  // one arrival per epilogue warp
         }
         for (int i = 0; i < 3; ++i) mbar_init(drain + i, 1);
+        for (int i = 0; i < kRowSlots; ++i) mbar_init(rows_ready + i, 8);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tQ);
@@ -629,7 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         cur = u;
                     }
                     const uint32_t uw = w ? uses1 : uses0, uo = w ? uses0 : uses1;
-                    if (uw > 0 && !mbar_wait(tmem_free + w, (uw - 1) & 1, p.status, 24, abort_flag))
+                    // The buffer's previous tile must be done with its columns: with k_pad <= 128
+                    // the scores cover P (consumed once its P.V is done) but not O (read by
+                    // the epilogue, which the next P.V into O waits for instead).
+                    if (uw > 0 && !mbar_wait(kLoHere ? o_full + w : tmem_free + w, (uw - 1) & 1, p.status,
+                                             24, abort_flag))
                         break;
                     if (terms == 3 && !kLoHere && uo > 0 &&
                         !mbar_wait(tmem_free + (w ^ 1), (uo - 1) & 1, p.status, 24, abort_flag))
@@ -696,6 +711,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait(v_full, (nv - 1) & 1, p.status, 23, abort_flag)) break;
                         fresh = false;
                     }
+                    // k_pad <= 128: O of the buffer's previous tile read by the epilogue
+                    if (kLoHere && j >= 2 &&
+                        !mbar_wait(tmem_free + w, ((j >> 1) - 1) & 1, p.status, 24, abort_flag))
+                        break;
                     tc_fence_after();
                     const uint32_t a = tmem + kBufCols * w + c0;          // P_half: 8 columns per step
                     // P_lo (three products): after the half's P, or in the other buffer
@@ -745,20 +764,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t oa[64];  // O of this row: both key halves, to the first half's maximum
             {
                 const int w = j & 1;
+                const int rs = kLoHere ? (j & (kRowSlots - 1)) : w;  // row maxima and sums
+                const uint32_t rpar = (uint32_t)(j / kRowSlots) & 1u;
                 ++j;
                 const uint32_t par = w ? par1 : par0;
-                ok = warp_wait(p_full + 2 * w, par, p.status, 27, abort_flag) &&
-                     warp_wait(p_full + 2 * w + 1, par, p.status, 27, abort_flag);
+                ok = kLoHere ? warp_wait(rows_ready + rs, rpar, p.status, 27, abort_flag)
+                             : warp_wait(p_full + 2 * w, par, p.status, 27, abort_flag) &&
+                                   warp_wait(p_full + 2 * w + 1, par, p.status, 27, abort_flag);
                 // Row = (O_a + g O_b) / (l_a + g l_b), g = 2^(m_b - m_a).  g is capped
                 // at 2^100: beyond that O_a's share is below fp32 resolution anyway,
                 // and O_b g stays finite (|O_b| < 2^21).
                 float g = 0.f;
                 if (ok) {
-                    l = rsum[(w * 2) * kTileM + tw];
+                    l = rsum[(rs * 2) * kTileM + tw];
                     if (has_b) {
-                        g = ex2_approx(fminf(rmax[(w * 2 + 1) * kTileM + tw] - rmax[(w * 2) * kTileM + tw],
+                        g = ex2_approx(fminf(rmax[(rs * 2 + 1) * kTileM + tw] - rmax[(rs * 2) * kTileM + tw],
                                              100.f));
-                        l = fmaf(rsum[(w * 2 + 1) * kTileM + tw], g, l);
+                        l = fmaf(rsum[(rs * 2 + 1) * kTileM + tw], g, l);
                     }
                     ok = warp_wait(o_full + w, par, p.status, 28, abort_flag);
                 }
@@ -859,11 +881,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float l = softmax_half<kLoHere>(tmem + lane_off + kBufCols * w,
                                          tmem + lane_off + kBufCols * (w ^ 1), c0, nch, p.k,
                                          p.scale_log2, wk.terms == 3, mb);
-            rsum[(w * 2 + h) * kTileM + tw] = l;
-            rmax[(w * 2 + h) * kTileM + tw] = mb;
+            const int rs = kLoHere ? (j & (kRowSlots - 1)) : w;
+            rsum[(rs * 2 + h) * kTileM + tw] = l;
+            rmax[(rs * 2 + h) * kTileM + tw] = mb;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + 2 * w + h);
+            if (lane == 0) {
+                mbar_arrive(p_full + 2 * w + h);
+                if (kLoHere) mbar_arrive(rows_ready + rs);
+            }
             ++j;
         }
     }
@@ -876,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 size_t attend_smem_bytes(int) {
-    return 1024 + 4 * kImg + kQSlots * kQBytes + 2 * kPiece + 2 * 2 * 2 * kTileM * sizeof(float) +
+    return 1024 + 4 * kImg + kQSlots * kQBytes + 2 * kPiece + 2 * kRowSlots * 2 * kTileM * sizeof(float) +
            256;
 }
 

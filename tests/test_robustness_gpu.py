@@ -217,6 +217,35 @@ def test_forwards_in_a_stream_see_inputs_written_between_them():
     assert torch.equal(O2, O3), "back-to-back forwards differ"
 
 
+@pytest.mark.parametrize("mode,k,forced", [(KV, 128, 0), (HEADWISE, 128, 3), (LAYERWISE, 256, 0)])
+def test_many_forwards_back_to_back(mode, k, forced):
+    """Hundreds of forwards in a row, each attention CTA working through many tiles: every
+    bounded device wait must be met (the device status stays clear) and every call must
+    give the same output.  With k_pad <= 128 a buffer's next score products wait only for
+    its previous P.V, so a softmax may finish a tile while the epilogue is two tiles
+    behind in the same buffer; a per-buffer barrier would then have run a phase past the
+    epilogue's wait (the row sums' own four-slot barriers prevent that)."""
+    b, h, n, d = 8, 12, 1024, 64
+    x = case_inputs(b, h, n, d, k, mode, BF16, seed=91)
+    g = to_device(x, DEV)
+
+    def fwd():
+        return lf.attention(g["Q"], g["K"], g["V"], g["E"], g["F"], g["lengths"], mode)
+
+    prev = lf.linformer_set_pv_terms(forced)  # 0: each unit's own choice
+    try:
+        O1 = fwd()
+        for _ in range(300):
+            O2 = fwd()
+        torch.cuda.synchronize()
+    finally:
+        lf.linformer_set_pv_terms(prev)
+    assert lf.linformer_debug_read_device_status() == 0
+    assert torch.equal(O1, O2), "repeated forwards differ"
+    check(host64(O1), orc.linformer_fwd(x["Q"], x["K"], x["V"], x["E"], x["F"], x["lengths"],
+                                        mode)[0], BF16, "first of the repeated forwards")
+
+
 def test_two_streams_and_the_projection_entry_point_interleaved():
     """Forwards on two streams at once (each stream's projection waits only for its own
     stream's previous kernel), and the projection-only entry point between forwards in
